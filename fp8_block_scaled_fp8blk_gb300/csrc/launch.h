@@ -1,0 +1,97 @@
+// launch.h -- host-side planning and launch entry points shared by the
+// libfp8blk translation units (not part of the public ABI).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "stream_gemv.cuh"
+
+namespace fp8blk {
+
+// Launch-shape knobs.  Results do not depend on them (each output's
+// reduction order is fixed by the column panel layout alone); only speed does.
+struct Tuning {
+    int target_stage_bytes = 32 * 1024;  // bytes of weights per pipeline stage
+    int ctas_per_sm = 0;                 // 0 = 2 for m <= 4, 1 for m > 4
+    int use_pdl = 1;                     // programmatic dependent launch
+    int l2_prefetch = 1;                 // L2 prefetch of the first stages before the PDL wait
+    int max_stages = kMaxStages;
+};
+Tuning &tuning();
+
+struct DeviceInfo {
+    int sms = 0;
+    int smem_per_sm = 0;      // bytes
+    int smem_per_block = 0;   // opt-in maximum, bytes
+    unsigned int *status = nullptr;  // device address of the status word
+};
+// Per-device facts, queried once per device (current device).
+cudaError_t current_device_info(DeviceInfo *out);
+
+// Geometry of one streaming-GEMV launch (see GemvArgs).
+struct Plan {
+    int panels = 1;
+    int panel_cols = 0;
+    int team_warps_log2 = 0;
+    int rb = 1;
+    int stage_rows = 0;
+    int stage_bytes = 0;
+    int stages = 2;
+    int ctas_per_sm = 1;
+    int64_t n_groups = 0;
+};
+constexpr int kStaticSmemReserve = 6 * 1024;  // red/argmax buffers + slack
+constexpr int kMaxGrid = 1024;               // bound on CTAs (argmax partials)
+
+// Plans a launch of m rows over a [rows, cols] matrix of bpw-byte weights.
+Plan make_plan(int m, int64_t rows, int64_t cols, int bpw, const DeviceInfo &dev);
+
+// Fill GemvArgs geometry from a plan.
+void apply_plan(const Plan &p, GemvArgs *a);
+
+// Kernel launches (defined in gemv_e4m3.cu / gemv_bf16.cu / nvfp4_dequant.cu).
+cudaError_t launch_gemv_e4m3(const GemvArgs &a, const Plan &p, int m, bool argmax,
+                             const DeviceInfo &dev, cudaStream_t stream);
+cudaError_t launch_gemv_bf16(const GemvArgs &a, const Plan &p, int m, const DeviceInfo &dev,
+                             cudaStream_t stream);
+cudaError_t launch_nvfp4_dequant(const uint8_t *codes, const uint8_t *scales, float g,
+                                 uint16_t *out, int64_t rows, int64_t cols,
+                                 const DeviceInfo &dev, cudaStream_t stream);
+
+// Resident CTAs per SM of `kernel` with `smem` dynamic shared memory on the
+// current device.  Raises the kernel's dynamic-smem limit first; both answers
+// are cached per (kernel, device, smem), so steady-state launches (and stream
+// capture) make no attribute or occupancy calls.
+cudaError_t kernel_occupancy(const void *kernel, size_t smem, int *per_sm);
+
+// Shared launcher: grid from occupancy, dynamic smem attribute, optional PDL.
+template <typename Kernel>
+cudaError_t launch_stream_kernel(Kernel kernel, const GemvArgs &a, const Plan &p,
+                                 const DeviceInfo &dev, cudaStream_t stream) {
+    const size_t smem = static_cast<size_t>(p.stages) * p.stage_bytes + kMaxStages * sizeof(uint64_t);
+    int per_sm = 0;
+    cudaError_t err = kernel_occupancy(reinterpret_cast<const void *>(kernel), smem, &per_sm);
+    if (err != cudaSuccess) return err;
+    if (per_sm < 1) return cudaErrorInvalidConfiguration;
+    if (per_sm > p.ctas_per_sm) per_sm = p.ctas_per_sm;
+    int64_t grid = static_cast<int64_t>(dev.sms) * per_sm;
+    if (grid > p.n_groups) grid = p.n_groups;
+    if (grid > kMaxGrid) grid = kMaxGrid;
+    if (grid < 1) grid = 1;
+
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(grid));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = tuning().use_pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kernel, a);
+}
+
+}  // namespace fp8blk

@@ -1,0 +1,211 @@
+/*
+ * fp8blk.h -- C ABI of libfp8blk: the GB300 (sm_103a) FP8 block-scaled decode
+ * GEMV, its fused greedy argmax, and the NVFP4 routed-expert dequant + GEMV.
+ *
+ * Conventions for every entry point
+ *   - Plain C types only.  `stream` is a cudaStream_t passed as void*
+ *     (NULL = the legacy default stream).
+ *   - Device pointers are CUDA device (or managed) memory owned by the caller.
+ *     The library allocates nothing, frees nothing and never synchronizes:
+ *     every GPU entry point only enqueues kernels on `stream` and returns.
+ *     Buffers must stay alive until that work has run.
+ *   - Arguments are checked on the host before anything is enqueued; on any
+ *     error nothing is launched and the return value says why.
+ *   - Matrices are row-major and dense (row stride = number of columns).
+ *   - Integer sizes are int64_t; the product rows * cols may exceed 2^31.
+ *
+ * Return codes (int): FP8BLK_OK on success, otherwise one of the codes below;
+ * fp8blk_strerror() names them.
+ */
+#ifndef FP8BLK_H
+#define FP8BLK_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define FP8BLK_OK 0
+#define FP8BLK_EINVAL 1  /* null pointer, size <= 0, m outside [1, 8], column count not a
+                            multiple of the format's granule, bad or repeated expert id */
+#define FP8BLK_EALIGN 2  /* a pointer is not aligned as documented */
+#define FP8BLK_ESCALE 3  /* e8m0 code 0xFF, or an NVFP4 global scale that is not a finite
+                            nonzero power of two (the bf16 dequant would not be exact) */
+#define FP8BLK_EWS 4     /* workspace missing or smaller than the *_ws_bytes() answer */
+#define FP8BLK_ECUDA 5   /* the CUDA runtime refused a launch or attribute call */
+#define FP8BLK_ERANGE 6  /* a size is beyond what the kernels index (rows >= 2^31, ...) */
+
+#define FP8BLK_MAX_M 8      /* activation rows per call: 1 (decode) .. 8 (batched verify) */
+#define FP8BLK_BLOCK 128    /* side of a square scale block */
+
+/* Bits of the device status word (see fp8blk_device_status). */
+#define FP8BLK_STATUS_WAIT_TIMEOUT 1u /* a kernel gave up waiting for a weight tile (bounded
+                                         wait, about one second); its outputs are invalid */
+
+/* Version of this ABI; bumped on any incompatible change. */
+int fp8blk_abi_version(void);
+
+/* Human-readable name of a return code (static storage). */
+const char *fp8blk_strerror(int code);
+
+/*
+ * fp8blk_scales_from_e8m0 -- HOST function: decode an e8m0 block-scale grid
+ * to f32, out[k] = 2^(codes[k] - 127).  Source: "Module dsv4_gpu" page,
+ * struct Fp8Dense (the 128x128 block-scale grid is decoded to f32 on the host;
+ * every e8m0 code is a power of two; 0xFF is refused at load).
+ *   codes      host, n bytes
+ *   out        host, n floats (code 0 decodes to the f32 subnormal 2^-127)
+ *   bad_index  host, optional: on FP8BLK_ESCALE receives the first 0xFF index
+ * Returns FP8BLK_ESCALE on any 0xFF code (out is then unspecified), EINVAL on
+ * null codes/out with n > 0.
+ */
+int fp8blk_scales_from_e8m0(const uint8_t *codes, size_t n, float *out, size_t *bad_index);
+
+/*
+ * fp8blk_gemv -- y[i][r] = sum_c e4m3(W[r][c]) * S[r/128][c/128] * x[i][c]
+ * for i < m, r < rows.  Source: "Module dsv4_gpu" page, struct Fp8Dense (the
+ * device GEMV decodes e4m3(code) * scale in-register) and "Struct Dsv4Gpu"
+ * page, field dense_fp8 (decode and verify read the FP8-blk linears as stored)
+ * and method verify_batch_dev (m = T = k+1 verify rows).
+ *   w_codes  device, uint8 e4m3 codes [rows, cols], 16-byte aligned.  NaN codes
+ *            (0x7F, 0xFF) are not refused; they make the affected outputs NaN.
+ *   scales   device, f32 grid [ceil(rows/128), ceil(cols/128)], 4-byte aligned
+ *            (normally the output of fp8blk_scales_from_e8m0).
+ *   x        device, f32 activations [m, cols], 16-byte aligned; used as f32.
+ *   y        device, f32 outputs [m, rows], 4-byte aligned; fully overwritten.
+ *            Must not overlap any input.
+ *   m        1..8;  rows >= 1;  cols >= 16 and a multiple of 16.
+ * Accumulation is f32 in a fixed order (results are deterministic run to
+ * run); each product is formed as e4m3 * (x * S), exact unless x * S leaves
+ * the f32 range.  Error bound versus the exact sum: |err| <= 1e-5 * sum|w x|
+ * + 1e-6 per output.
+ * Errors: EINVAL, EALIGN, ERANGE (rows or cols >= 2^31), ECUDA.
+ */
+int fp8blk_gemv(const uint8_t *w_codes, const float *scales, const float *x, float *y, int m,
+                int64_t rows, int64_t cols, void *stream);
+
+/*
+ * fp8blk_gemv_argmax_ws_bytes -- workspace size (bytes) that
+ * fp8blk_gemv_argmax needs for this shape.  Returns 0 for invalid shapes.
+ */
+size_t fp8blk_gemv_argmax_ws_bytes(int m, int64_t rows, int64_t cols);
+
+/*
+ * fp8blk_gemv_argmax -- the same GEMV fused with a greedy argmax per
+ * activation row: tokens[i] = min{ r : y[i][r] = max_r' y[i][r'] }.
+ * Source: "Struct Dsv4Gpu" page, method decode_step_greedy (the argmax runs on
+ * the device and only 4 bytes cross back) and method verify_batch_dev (a
+ * per-position argmax [T]); "dflash.rs source" page, fn dflash2_walk_greedy
+ * (ascending scan with a strict '>': the lowest index wins ties).
+ * NaN never wins; -0 and +0 tie; a row with nothing above -inf gives token 0.
+ * The token is the argmax of the f32 logits this call computes (the same
+ * values written to `logits` when it is given).
+ *   logits   device, optional (NULL = not written): f32 [m, rows], 4-aligned
+ *   tokens   device, uint32 [m], 4-byte aligned; the caller copies it back
+ *   ws       device workspace of at least fp8blk_gemv_argmax_ws_bytes(m, rows,
+ *            cols) bytes, 16-byte aligned.  It must be zero-filled once
+ *            before its first use; every call leaves it ready for the next.
+ *            Calls that share a workspace must be ordered (same stream).
+ *   others   as fp8blk_gemv.
+ * Errors: as fp8blk_gemv, plus EWS.
+ */
+int fp8blk_gemv_argmax(const uint8_t *w_codes, const float *scales, const float *x,
+                       float *logits, uint32_t *tokens, void *ws, size_t ws_bytes, int m,
+                       int64_t rows, int64_t cols, void *stream);
+
+/*
+ * fp8blk_bf16_gemv -- y[i][r] = sum_c bf16(B[r][c]) * x[i][c], f32
+ * accumulation.  The GEMV that follows the per-expert dequant.  Source:
+ * "Module dsv4_gpu" page, module header (bf16 GEMMs with f32 accumulation)
+ * and enum ExpertArm (Bf16Dequant).  x stays f32.
+ *   w_bf16   device, bf16 bit patterns [rows, cols], 16-byte aligned
+ *   x, y, m  as fp8blk_gemv;  cols >= 16 and a multiple of 16.
+ * Errors: EINVAL, EALIGN, ERANGE, ECUDA.
+ */
+int fp8blk_bf16_gemv(const uint16_t *w_bf16, const float *x, float *y, int m, int64_t rows,
+                     int64_t cols, void *stream);
+
+/*
+ * nvfp4_expert_dequant -- dequantise one NVFP4 expert to bf16:
+ *   out[r][c] = bf16( e2m1(q[r][c]) * e4m3(s[r][c/16]) * g[e] ),
+ * exact in bf16 (the host refuses global scales for which it would not be).
+ * Source: "Module dsv4_gpu" page, module header and enum ExpertArm (routed
+ * experts stay NVFP4 as stored and each activated expert is dequantised into a
+ * reused bf16 scratch, exact in bf16) and enum ExpertKind (trunk = NVFP4).
+ *   codes        device, uint8 [n_experts, rows, cols/2], two e2m1 codes per
+ *                byte, column 2j in the LOW nibble; 16-byte aligned
+ *   scales       device, uint8 e4m3 [n_experts, rows, cols/16], 2-byte aligned
+ *   gscale_host  HOST, f32 [n_experts]: per-expert global scale, each a finite
+ *                nonzero power of two (else ESCALE)
+ *   expert_id    0 <= expert_id < n_experts
+ *   out          device, uint16 bf16 bits [rows, cols], 16-byte aligned
+ *   cols         a multiple of 32.
+ * Errors: EINVAL, EALIGN, ESCALE, ERANGE, ECUDA.
+ */
+int nvfp4_expert_dequant(const uint8_t *codes, const uint8_t *scales, const float *gscale_host,
+                         int n_experts, int expert_id, uint16_t *out, int64_t rows, int64_t cols,
+                         void *stream);
+
+/*
+ * nvfp4_expert_dequant_gemv -- for k < n_active: dequantise expert
+ * ids_host[k] into the reused bf16 scratch, then y[k] = scratch x.
+ * Same sources as nvfp4_expert_dequant.  The scratch is reused in stream
+ * order; when the call's work has run it holds the LAST active expert.
+ *   ids_host     HOST, int32 [n_active], distinct, each in [0, n_experts)
+ *   n_active     >= 1
+ *   x            device, f32 [cols], 16-byte aligned
+ *   y            device, f32 [n_active, rows], 4-byte aligned
+ *   bf16_scratch device, uint16 [rows, cols], 16-byte aligned
+ *   others       as nvfp4_expert_dequant.
+ * Errors: as nvfp4_expert_dequant.
+ */
+int nvfp4_expert_dequant_gemv(const uint8_t *codes, const uint8_t *scales,
+                              const float *gscale_host, int n_experts, const int32_t *ids_host,
+                              int n_active, const float *x, float *y, uint16_t *bf16_scratch,
+                              int64_t rows, int64_t cols, void *stream);
+
+/*
+ * fp8blk_set_launch_tuning -- process-wide launch-shape knobs for the
+ * streaming GEMV kernels.  They change speed only: every output is reduced in
+ * an order fixed by the column panel layout, so results are bit-identical
+ * under any setting.  Pass 0 for a knob's default.
+ *   target_stage_bytes  weight bytes per shared-memory pipeline stage (32 KiB)
+ *   ctas_per_sm         resident CTAs per SM, 1..4 (2 for m <= 4, else 1)
+ *   use_pdl             programmatic dependent launch on (nonzero) or off
+ *   l2_prefetch         L2 prefetch of the first stages before the grid
+ *                       dependency wait, on (nonzero) or off
+ *   max_stages          pipeline depth cap, 2..8 (8)
+ * Not thread-safe against concurrent calls of the other entry points.
+ * Errors: EINVAL.
+ */
+int fp8blk_set_launch_tuning(int target_stage_bytes, int ctas_per_sm, int use_pdl, int l2_prefetch,
+                             int max_stages);
+
+/*
+ * fp8blk_plan_query -- HOST, no CUDA calls: the launch geometry the streaming
+ * GEMV would use for this shape on a device with the given SM count and
+ * shared-memory limits (bytes), for inspection and bounds checks.
+ *   bytes_per_weight  1 (e4m3) or 2 (bf16)
+ *   out  host int64[12]: panels, panel_cols, team_warps, teams, row_batches,
+ *        rows_per_batch, stage_rows, stage_bytes, stages, ctas_per_sm,
+ *        n_groups, dynamic_smem_bytes
+ * Errors: EINVAL (bad shape or device facts).
+ */
+int fp8blk_plan_query(int m, int64_t rows, int64_t cols, int bytes_per_weight, int sms,
+                      int smem_per_sm, int smem_per_block, int64_t *out);
+
+/*
+ * fp8blk_device_status -- read (and optionally clear) the library's device
+ * status word on the current device (FP8BLK_STATUS_* bits; 0 = healthy).
+ * SYNCHRONIZES the current device.  status_out is a host pointer.
+ * Errors: EINVAL, ECUDA.
+ */
+int fp8blk_device_status(uint32_t *status_out, int clear);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FP8BLK_H */
