@@ -1,0 +1,522 @@
+#!/usr/bin/env python3
+"""Benchmark of the FP8-blk decode GEMV hot path on GB300.
+
+Headline workload: the FP8-blk dense-linear GEMV, W 4096 x 4096 e4m3 codes with
+a 32 x 32 grid of e8m0 block scales (decoded to f32 on the host), x f32 [1, 4096],
+y f32 [1, 4096].  One step = one fp8blk_gemv call (one kernel launch) on one
+weight matrix with one activation row.  Weights, scales and x are resident in
+HBM before the timed region; the timed region replays CUDA graphs of
+back-to-back calls that rotate over enough distinct weight copies that their
+total exceeds L2 (so every call streams its weights from HBM).
+
+Metric: algorithmic bytes (codes + f32 scales + activations + outputs) per
+second, GB/s, and its fraction of the measured HBM peak; microseconds per call.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+--impl reference times the plain CPU oracle on this host on bounded row
+samples of the same workload (the only other place this script runs the oracle
+is the cpu_baseline leg).  Under torchrun (N > 1) every rank runs an
+independent replica on its own GPU (weak scaling, no data-path collective);
+rank 0 prints the JSON line.
+"""
+from __future__ import annotations
+
+import argparse
+import datetime as _dt
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "FP8-blk decode GEMV weight GB/s (fraction of GB300 HBM peak); us per call"
+HEADLINE = "gemv_4096x4096_m1"
+L2_BYTES = 129 * 1024 * 1024
+FALLBACK_HBM_GBS = 6800.0
+CSRC = os.path.join(ROOT, "fp8_block_scaled_fp8blk_gb300", "csrc")
+
+
+# ---------------------------------------------------------------- byte counts
+def fp8blk_bytes(rows: int, cols: int, m: int, argmax: bool = False) -> int:
+    """codes + f32 scale grid + activations + outputs (tokens for argmax)."""
+    grid = math.ceil(rows / 128) * math.ceil(cols / 128) * 4
+    out = m * 4 if argmax else m * rows * 4
+    return rows * cols + grid + m * cols * 4 + out
+
+
+def nvfp4_bytes(n_active: int, rows: int, cols: int) -> int:
+    """Per active expert: e2m1 codes + e4m3 scales + f32 global scale; + x + y."""
+    per = rows * cols // 2 + rows * cols // 16 + 4
+    return n_active * per + cols * 4 + n_active * rows * 4
+
+
+def source_hash() -> str:
+    h = hashlib.sha1()
+    for name in sorted(os.listdir(CSRC)):
+        with open(os.path.join(CSRC, name), "rb") as f:
+            h.update(name.encode())
+            h.update(f.read())
+    return h.hexdigest()[:12]
+
+
+def hbm_peak() -> tuple[float, str]:
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured (MEASURED_PEAKS.json hbm_gbs)"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback (6.8 TB/s earlier GB300 copy measurement)"
+
+
+def profiled_traffic(workload: str):
+    """DRAM bytes per launch from a committed ncu summary, if it matches the
+    current kernel sources; else None."""
+    p = os.path.join(ROOT, "profiles", "ncu_traffic.txt")
+    if not os.path.exists(p):
+        return None
+    cur = source_hash()
+    with open(p) as f:
+        for line in f:
+            parts = line.split()
+            if len(parts) >= 3 and not line.startswith("#") and parts[0] == workload and parts[1] == cur:
+                return int(parts[2])
+    return None
+
+
+# ---------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi samples (every 50 ms) around the timed region."""
+
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    REASONS = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+
+    def __init__(self, uuid: str | None):
+        self.samples = []
+        self.error = None
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+               "-lms", "50"]
+        if uuid:
+            cmd.insert(1, f"--id={uuid}")
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                                         text=True, bufsize=1)
+        except Exception as e:  # nvidia-smi missing
+            self.proc, self.error = None, str(e)
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                ts = _dt.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                self.samples.append(dict(t=ts, sm=float(parts[1]), sm_max=float(parts[2]),
+                                         power=float(parts[3]) if parts[3] not in ("[N/A]", "N/A") else None,
+                                         reasons={r: parts[5 + k] == "Active"
+                                                  for k, r in enumerate(self.REASONS)}))
+            except ValueError:
+                continue
+
+    def stop(self):
+        if self.proc is not None:
+            time.sleep(0.15)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.thread.join(timeout=5)
+
+    def summary(self, t0: float, t1: float) -> dict:
+        if self.proc is None:
+            return {"error": self.error or "nvidia-smi unavailable"}
+        inside = [s for s in self.samples if t0 <= s["t"] <= t1]
+        note = "samples inside the timed region"
+        if not inside and self.samples:
+            inside = sorted(self.samples, key=lambda s: abs(s["t"] - 0.5 * (t0 + t1)))[:2]
+            note = "timed region shorter than the sampling period: nearest samples"
+        if not inside:
+            return {"error": "no nvidia-smi samples"}
+        reasons = sorted({r for s in inside for r, on in s["reasons"].items() if on})
+        powers = [s["power"] for s in inside if s["power"] is not None]
+        return {"sm_mhz": statistics.median(s["sm"] for s in inside),
+                "sm_max_mhz": max(s["sm_max"] for s in inside),
+                "reasons": reasons, "samples": len(inside), "note": note,
+                "power_w_max": max(powers) if powers else None}
+
+
+# ---------------------------------------------------------------- distributed
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def max_over_ranks(value: float, world: int, device) -> float:
+    if world == 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ---------------------------------------------------------------- timing core
+def time_graphed(calls, steps: int, warmup: int, stream, world: int, device, sampler=None,
+                 per_graph: int = 1000):
+    """Run `warmup` eager calls, then exactly `steps` calls replayed from CUDA
+    graphs on `stream`; returns (elapsed ms over the steps, max over ranks,
+    host window)."""
+    import torch
+    n = len(calls)
+    with torch.cuda.stream(stream):
+        for i in range(max(warmup, 3)):
+            calls[i % n]()
+    stream.synchronize()
+
+    def capture(count):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for i in range(count):
+                calls[i % n]()
+        return g
+
+    per_graph = max(n, (per_graph // n) * n)
+    full, rem = divmod(steps, per_graph)
+    g_full = capture(per_graph) if full else None
+    g_rem = capture(rem) if rem else None
+    with torch.cuda.stream(stream):  # warm the graphs themselves (untimed)
+        if g_full is not None:
+            g_full.replay()
+        if g_rem is not None:
+            g_rem.replay()
+    stream.synchronize()
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    barrier(world)
+    torch.cuda.synchronize()
+    t0 = time.time()
+    with torch.cuda.stream(stream):
+        start.record(stream)
+        for _ in range(full):
+            g_full.replay()
+        if g_rem is not None:
+            g_rem.replay()
+        end.record(stream)
+    torch.cuda.synchronize()
+    t1 = time.time()
+    barrier(world)
+    ms = start.elapsed_time(end)
+    return max_over_ranks(ms, world, device), (t0, t1)
+
+
+# ---------------------------------------------------------------- workloads
+def up(a, device, dtype=None):
+    import numpy as np
+    import torch
+    t = torch.from_numpy(np.ascontiguousarray(a))
+    if dtype is not None:
+        t = t.view(dtype)
+    return t.to(device)
+
+
+def copies_for(nbytes: int) -> int:
+    return max(2, math.ceil(2.5 * L2_BYTES / nbytes))
+
+
+def setup_fp8blk(name: str, device, argmax: bool = False):
+    import torch
+    from fp8_block_scaled_fp8blk_gb300 import ops, synth
+    w = synth.WORKLOADS[name]
+    rows, cols, m = w["rows"], w["cols"], w["m"]
+    case = synth.workload_case(name)
+    s = up(ops.fp8blk_scales_from_e8m0(case.scale_e8m0), device)
+    w0 = up(case.codes, device)
+    n = copies_for(rows * cols)
+    ws_ = [w0] + [w0.clone() for _ in range(n - 1)]
+    x = up(case.x, device)
+    calls = []
+    if argmax:
+        wsp = [ops.argmax_workspace(m, rows, cols, device) for _ in range(n)]
+        toks = [torch.empty(m, dtype=torch.int32, device=device) for _ in range(n)]
+        for i in range(n):
+            calls.append(lambda i=i: ops.fp8blk_gemv_argmax(ws_[i], s, x, wsp[i], tokens=toks[i]))
+    else:
+        ys = [torch.empty((m, rows), dtype=torch.float32, device=device) for _ in range(n)]
+        for i in range(n):
+            calls.append(lambda i=i: ops.fp8blk_gemv(ws_[i], s, x, y=ys[i]))
+    return dict(case=case, calls=calls, copies=n, rows=rows, cols=cols, m=m, weights=ws_, scales=s,
+                bytes=fp8blk_bytes(rows, cols, m, argmax))
+
+
+def setup_nvfp4(device):
+    import numpy as np
+    import torch
+    from fp8_block_scaled_fp8blk_gb300 import ops, synth
+    w = synth.NVFP4_WORKLOAD
+    c = synth.nvfp4_case(w["n_experts"], w["rows"], w["cols"], w["n_active"], w["seed"])
+    codes, scales, x = up(c.codes, device), up(c.scales, device), up(c.x, device)
+    rows, cols = w["rows"], w["cols"]
+    rng = np.random.default_rng(w["seed"] + 100)
+    id_sets = [c.ids] + [rng.choice(w["n_experts"], w["n_active"], replace=False).astype(np.int32)
+                         for _ in range(9)]
+    scratch = torch.empty((rows, cols), dtype=torch.int16, device=device)
+    ys = [torch.empty((w["n_active"], rows), dtype=torch.float32, device=device) for _ in id_sets]
+    calls = [lambda i=i: ops.nvfp4_expert_dequant_gemv(codes, scales, c.gscale, id_sets[i], x,
+                                                       scratch, y=ys[i]) for i in range(len(id_sets))]
+    return dict(calls=calls, bytes=nvfp4_bytes(w["n_active"], rows, cols), launches=2 * w["n_active"])
+
+
+def measure_extra(device, stream, world, peak):
+    """The other workloads of the path, measured the same way (one JSON line)."""
+    out = {}
+    for name, argmax, steps in (("gemv_512x1024_m1", False, 4000),
+                                ("head_argmax_131072x4096_m1", True, 300),
+                                ("verify_16384x4096_m8", False, 2000)):
+        st = setup_fp8blk(name, device, argmax)
+        ms, _ = time_graphed(st["calls"], steps, 20, stream, world, device,
+                             per_graph=200 if argmax else 1000)
+        us = ms * 1e3 / steps
+        gbs = st["bytes"] / (us * 1e-6) / 1e9
+        out[name] = {"us_per_call": round(us, 3), "gbs": round(gbs, 1),
+                     "frac_of_hbm_peak": round(gbs / peak, 4), "bytes_per_call": st["bytes"],
+                     "weight_copies": st["copies"], "steps": steps}
+        del st
+    st = setup_nvfp4(device)
+    steps = 500
+    ms, _ = time_graphed(st["calls"], steps, 20, stream, world, device, per_graph=100)
+    us = ms * 1e3 / steps
+    gbs = st["bytes"] / (us * 1e-6) / 1e9
+    out["nvfp4_experts_6of64_2048x4096"] = {
+        "us_per_call": round(us, 3), "gbs": round(gbs, 1), "frac_of_hbm_peak": round(gbs / peak, 4),
+        "bytes_per_call": st["bytes"], "launches_per_call": st["launches"], "steps": steps,
+        "note": "algorithmic bytes exclude the 2 x 16 MiB bf16 scratch write+read per expert"}
+    return out
+
+
+def measure_e2e(st, steps: int, device) -> dict:
+    """Same metric through the public API with host buffers: per step, copy x
+    from pinned host memory, run the GEMV, read y back, synchronize."""
+    import torch
+    from fp8_block_scaled_fp8blk_gb300 import ops
+    case = st["case"]
+    x_h = torch.from_numpy(case.x.copy()).pin_memory()
+    y_h = torch.empty((st["m"], st["rows"]), dtype=torch.float32).pin_memory()
+    x_d = torch.empty_like(x_h, device=device)
+    y_d = torch.empty((st["m"], st["rows"]), dtype=torch.float32, device=device)
+    s = st["scales"]
+    n = len(st["weights"])
+    stream = torch.cuda.current_stream(device)
+
+    def one(i):
+        x_d.copy_(x_h, non_blocking=True)
+        ops.fp8blk_gemv(st["weights"][i % n], s, x_d, y=y_d)
+        y_h.copy_(y_d, non_blocking=True)
+        stream.synchronize()
+
+    for i in range(20):
+        one(i)
+    k = max(1, min(steps, 20000))
+    t0 = time.perf_counter()
+    for i in range(k):
+        one(i)
+    dt = (time.perf_counter() - t0) / k
+    return {"value": round(st["bytes"] / dt / 1e9, 2), "unit": "GB/s", "us_per_call": round(dt * 1e6, 3),
+            "steps": k, "h2d_bytes_per_step": x_h.numel() * 4, "d2h_bytes_per_step": y_h.numel() * 4}
+
+
+def cpu_baseline(name: str, budget_s: float = 8.0) -> dict:
+    """The oracle, as it stands, on this host's cores: whole GEMV calls of the
+    same workload for about budget_s seconds."""
+    import oracle
+    from fp8_block_scaled_fp8blk_gb300 import synth
+    w = synth.WORKLOADS[name]
+    case = synth.workload_case(name)
+    cores = os.cpu_count() or 1
+    oracle.build()
+    t0 = time.perf_counter()
+    n = 0
+    while True:
+        oracle.fp8blk_gemv(case.codes, case.scale_e8m0, case.x, nthreads=cores)
+        n += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s:
+            break
+    nbytes = fp8blk_bytes(w["rows"], w["cols"], w["m"])
+    return {"value": round(nbytes * n / el / 1e9, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+            "sample": f"{n} whole {w['rows']}x{w['cols']} m={w['m']} calls in {el:.1f} s "
+                      f"(double-precision oracle, {cores} threads)"}
+
+
+# ---------------------------------------------------------------- arms
+def run_ours(args):
+    import torch
+    world, rank, local = dist_setup()
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=device)
+    from fp8_block_scaled_fp8blk_gb300 import ops
+    peak, peak_src = hbm_peak()
+    stream = torch.cuda.Stream(device)
+    st = setup_fp8blk(HEADLINE, device)
+    try:
+        uuid = str(torch.cuda.get_device_properties(device).uuid)
+        uuid = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+    except Exception:
+        uuid = None
+    sampler = ClockSampler(uuid) if rank == 0 else None
+    time.sleep(0.3)
+    ms, (t0, t1) = time_graphed(st["calls"], args.steps, args.warmup, stream, world, device)
+    clocks = sampler.summary(t0, t1) if sampler else None
+    if sampler:
+        sampler.stop()
+    us = ms * 1e3 / args.steps
+    per_gpu_gbs = st["bytes"] / (us * 1e-6) / 1e9
+    value = world * per_gpu_gbs
+    status = ops.fp8blk_device_status()
+    e2e = measure_e2e(st, args.steps, device)
+    e2e["value"] = round(e2e["value"] * world, 2) if world > 1 else e2e["value"]
+    extra = None
+    if world == 1 and not args.no_extra:
+        extra = measure_extra(device, stream, world, peak)
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(HEADLINE)
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms / args.steps, 6),
+            "us_per_call": round(us, 4), "frac_of_hbm_peak": round(per_gpu_gbs / peak, 4),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic (seeded numpy: e4m3 codes uniform over finite codes, e8m0 2^[-8,0], x N(0,1))",
+            "config": {"workload": HEADLINE, "rows": st["rows"], "cols": st["cols"], "m": st["m"],
+                       "weights": "e4m3 codes + 128x128 f32 block scales (from e8m0)",
+                       "bytes_per_call": st["bytes"], "weight_copies": st["copies"],
+                       "l2": f"inputs larger than L2: {st['copies']} rotating weight copies "
+                             f"({st['copies'] * st['rows'] * st['cols'] / 2**20:.0f} MiB)",
+                       "timing": "CUDA graphs of back-to-back calls, CUDA events on the launch stream",
+                       "parallelism": f"replicas x{world}"},
+            "roofline": {"bound": "hbm", "achieved": round(per_gpu_gbs, 1), "peak": peak, "unit": "GB/s",
+                         "frac": round(per_gpu_gbs / peak, 4), "traffic": profiled_traffic(HEADLINE),
+                         "peak_source": peak_src, "kernel": "stream_gemv_kernel<1,e4m3,false>",
+                         "algorithmic_bytes_per_launch": st["bytes"]},
+            "e2e": e2e,
+            "gpu_launches": args.steps,
+            "clocks": clocks,
+            "device_status": status,
+            "kernel_source_hash": source_hash(),
+        }
+        if cpu is not None:
+            line["cpu_baseline"] = cpu
+        if extra is not None:
+            line["workloads"] = extra
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def run_reference(args):
+    """The oracle on this host's cores, K steps of a bounded row sample each."""
+    world, rank, _ = dist_setup()
+    if rank != 0:
+        return
+    import oracle
+    from fp8_block_scaled_fp8blk_gb300 import synth
+    w = synth.WORKLOADS[HEADLINE]
+    rows, cols, m = w["rows"], w["cols"], w["m"]
+    case = synth.workload_case(HEADLINE)
+    cores = os.cpu_count() or 1
+    oracle.build()
+    t0 = time.perf_counter()
+    oracle.fp8blk_gemv(case.codes[:128], case.scale_e8m0[:1], case.x, nthreads=cores)
+    per_row = (time.perf_counter() - t0) / 128
+    budget = 90.0 / max(1, args.steps + args.warmup)
+    sample_rows = int(min(rows, max(1, budget / max(per_row, 1e-9))))
+    if sample_rows >= 128:
+        sample_rows -= sample_rows % 128
+    nblk = math.ceil(rows / 128)
+
+    def step(i):
+        b = i % nblk
+        r0 = b * 128
+        if sample_rows >= 128:
+            r0 = (i * sample_rows) % rows
+            r0 -= r0 % 128
+            r1 = min(rows, r0 + sample_rows)
+        else:
+            r1 = r0 + sample_rows
+        oracle.fp8blk_gemv(case.codes[r0:r1], case.scale_e8m0[r0 // 128:math.ceil(r1 / 128)], case.x,
+                           nthreads=cores)
+        return r1 - r0
+
+    for i in range(args.warmup):
+        step(i)
+    done = 0
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        done += step(i)
+    el = time.perf_counter() - t0
+    per_step_rows = done / args.steps
+    nbytes = per_step_rows * cols + math.ceil(per_step_rows / 128) * math.ceil(cols / 128) * 4 \
+        + m * cols * 4 + m * per_step_rows * 4
+    value = nbytes * args.steps / el / 1e9
+    line = {
+        "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(el * 1e3 / args.steps, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded numpy, same generator as the GPU arm)",
+        "config": {"workload": HEADLINE, "rows": rows, "cols": cols, "m": m,
+                   "sample_rows_per_step": sample_rows},
+        "impl": "reference",
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+                         "sample": f"{sample_rows} of {rows} rows per step, {args.steps} steps"},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200000)
+    ap.add_argument("--warmup", type=int, default=2000)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--no-extra", action="store_true", help="skip the other workloads")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -2,6 +2,7 @@
 // host-side argument checks, launch planning, and the device status word.
 // Nothing here allocates device memory or synchronizes, except
 // fp8blk_device_status, which is documented to synchronize.
+#include <algorithm>
 #include <cmath>
 #include <cstring>
 #include <map>
@@ -48,23 +49,30 @@ cudaError_t current_device_info(DeviceInfo *out) {
     return cudaSuccess;
 }
 
-cudaError_t kernel_occupancy(const void *kernel, size_t smem, int *per_sm) {
+cudaError_t kernel_occupancy(const void *kernel, int threads, size_t smem, int *per_sm) {
+    // The dynamic-smem limit is one value per (kernel, device): only ever
+    // raise it, so a smaller request never undercuts a cached larger one.
     static std::mutex mu;
+    static std::map<std::pair<const void *, int>, size_t> limit;
     static std::map<std::tuple<const void *, int, size_t>, int> cache;
     int dev = 0;
     cudaError_t err = cudaGetDevice(&dev);
     if (err != cudaSuccess) return err;
-    const auto key = std::make_tuple(kernel, dev, smem);
     std::lock_guard<std::mutex> lock(mu);
+    size_t &lim = limit[std::make_pair(kernel, dev)];
+    if (smem > lim) {
+        err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+        if (err != cudaSuccess) return err;
+        lim = smem;
+    }
+    const auto key = std::make_tuple(kernel, dev, smem);
     auto it = cache.find(key);
     if (it != cache.end()) {
         *per_sm = it->second;
         return cudaSuccess;
     }
-    err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
-    if (err != cudaSuccess) return err;
     int n = 0;
-    err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, kThreads, smem);
+    err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, threads, smem);
     if (err != cudaSuccess) return err;
     cache[key] = n;
     *per_sm = n;
@@ -87,6 +95,34 @@ Plan make_plan(int m, int64_t rows, int64_t cols, int bpw, const DeviceInfo &dev
     const int64_t per = (cols + panels0 - 1) / panels0;
     p.panel_cols = static_cast<int>((per + 15) / 16 * 16);
     p.panels = static_cast<int>((cols + p.panel_cols - 1) / p.panel_cols);
+    if (m == 1) {
+        // Row-per-warp kernel: each warp streams whole panel rows through a
+        // private ring; stages of about target/4 bytes, shrunk while there
+        // are fewer row groups than warps.
+        p.kind = kRowWarpKernel;
+        p.team_warps_log2 = 0;
+        p.rb = 1;
+        p.ctas_per_sm = t.ctas_per_sm > 0 ? t.ctas_per_sm : 2;
+        const int panel_bytes = p.panel_cols * bpw;
+        int rw = pow2_floor(std::max(1, (t.target_stage_bytes / 4) / panel_bytes));
+        if (rw > 8) rw = 8;
+        const int64_t warps = static_cast<int64_t>(dev.sms) * p.ctas_per_sm * kRowWarps;
+        while (rw > 1 && (rows + rw - 1) / rw < warps) rw /= 2;
+        int per_warp = dev.smem_per_sm / p.ctas_per_sm - 1024 - kStaticSmemReserve;
+        const int block_cap = dev.smem_per_block - kStaticSmemReserve;
+        if (per_warp > block_cap) per_warp = block_cap;
+        per_warp /= kRowWarps;
+        while (rw > 1 && 2 * rw * panel_bytes > per_warp) rw /= 2;
+        p.stage_rows = rw;
+        p.stage_bytes = rw * panel_bytes;
+        int stages = per_warp / p.stage_bytes;
+        if (stages > t.max_stages) stages = t.max_stages;
+        if (stages > kMaxStages) stages = kMaxStages;
+        if (stages < 2) stages = 2;
+        p.stages = stages;
+        p.n_groups = (rows + rw - 1) / rw;
+        return p;
+    }
     // One thread per 16 columns; a team is the power-of-two warp count that
     // covers a panel row; the CTA's 8 warps form 8 / team_warps teams.
     const int need_threads = (p.panel_cols + 15) / 16;
@@ -388,16 +424,17 @@ int fp8blk_plan_query(int m, int64_t rows, int64_t cols, int bytes_per_weight, i
     const int team_warps = 1 << p.team_warps_log2;
     out[0] = p.panels;
     out[1] = p.panel_cols;
-    out[2] = team_warps;
-    out[3] = kWarps / team_warps;
+    out[2] = p.kind == kRowWarpKernel ? 1 : team_warps;
+    out[3] = p.kind == kRowWarpKernel ? kRowWarps : kWarps / team_warps;
     out[4] = p.rb;
-    out[5] = 8 / pow2_ceil(m);
+    out[5] = p.kind == kRowWarpKernel ? 1 : 8 / pow2_ceil(m);
     out[6] = p.stage_rows;
     out[7] = p.stage_bytes;
     out[8] = p.stages;
     out[9] = p.ctas_per_sm;
     out[10] = p.n_groups;
-    out[11] = static_cast<int64_t>(p.stages) * p.stage_bytes + kMaxStages * static_cast<int64_t>(sizeof(uint64_t));
+    out[11] = static_cast<int64_t>(plan_smem_bytes(p));
+    out[12] = p.kind;
     return FP8BLK_OK;
 }
 

@@ -42,14 +42,19 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t byt
                  : "memory");
 }
 
+// Test-and-sleep: returns true once phase `parity` has completed; otherwise
+// the thread sleeps up to kSuspendHintNs (or less, at the hardware's choice)
+// without occupying issue slots, then returns false.
+constexpr uint32_t kSuspendHintNs = 100000;
+
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     uint32_t ok;
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
+        "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2, %3;\n\t"
         "selp.u32 %0, 1, 0, p;\n\t}"
         : "=r"(ok)
-        : "r"(bar), "r"(parity)
+        : "r"(bar), "r"(parity), "n"(kSuspendHintNs)
         : "memory");
     return ok != 0;
 }
@@ -60,11 +65,29 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity)
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = global_timer_ns();
     while (true) {
-#pragma unroll 1
-        for (int k = 0; k < 32; ++k)
-            if (mbar_try_wait(bar, parity)) return true;
+        if (mbar_try_wait(bar, parity)) return true;
         if (global_timer_ns() - t0 > kWaitLimitNs) return false;
     }
+}
+
+// Plain arrive (release) on a barrier, e.g. "this warp is done with a stage".
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+// Named barrier `id` over `nthreads` threads that also ORs a per-thread flag:
+// every participant gets the same answer.
+__device__ __forceinline__ bool bar_sync_or(int id, int nthreads, bool flag) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred q, p;\n\t"
+        "setp.ne.u32 q, %1, 0;\n\t"
+        "barrier.cta.red.or.pred p, %2, %3, q;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(r)
+        : "r"(static_cast<uint32_t>(flag)), "r"(id), "r"(nthreads)
+        : "memory");
+    return r != 0;
 }
 
 // ---------------------------------------------------------------- bulk copy

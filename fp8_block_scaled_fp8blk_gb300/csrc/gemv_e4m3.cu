@@ -13,8 +13,11 @@ static cudaError_t launch_m(const GemvArgs &a, const Plan &p, bool argmax, const
 
 cudaError_t launch_gemv_e4m3(const GemvArgs &a, const Plan &p, int m, bool argmax,
                              const DeviceInfo &dev, cudaStream_t stream) {
+    if (p.kind == kRowWarpKernel) {
+        if (argmax) return launch_stream_kernel(rowwarp_gemv_kernel<kE4M3, true>, a, p, dev, stream);
+        return launch_stream_kernel(rowwarp_gemv_kernel<kE4M3, false>, a, p, dev, stream);
+    }
     switch (m) {
-        case 1: return launch_m<1>(a, p, argmax, dev, stream);
         case 2: return launch_m<2>(a, p, argmax, dev, stream);
         case 3: return launch_m<3>(a, p, argmax, dev, stream);
         case 4: return launch_m<4>(a, p, argmax, dev, stream);

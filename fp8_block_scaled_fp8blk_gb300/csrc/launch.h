@@ -6,6 +6,7 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include "rowwarp_gemv.cuh"
 #include "stream_gemv.cuh"
 
 namespace fp8blk {
@@ -31,7 +32,9 @@ struct DeviceInfo {
 cudaError_t current_device_info(DeviceInfo *out);
 
 // Geometry of one streaming-GEMV launch (see GemvArgs).
+enum PlanKind : int { kTeamKernel = 0, kRowWarpKernel = 1 };
 struct Plan {
+    int kind = kTeamKernel;  // m = 1 uses the row-per-warp kernel
     int panels = 1;
     int panel_cols = 0;
     int team_warps_log2 = 0;
@@ -64,26 +67,34 @@ cudaError_t launch_nvfp4_dequant(const uint8_t *codes, const uint8_t *scales, fl
 // current device.  Raises the kernel's dynamic-smem limit first; both answers
 // are cached per (kernel, device, smem), so steady-state launches (and stream
 // capture) make no attribute or occupancy calls.
-cudaError_t kernel_occupancy(const void *kernel, size_t smem, int *per_sm);
+cudaError_t kernel_occupancy(const void *kernel, int threads, size_t smem, int *per_sm);
+
+// Dynamic shared memory of a planned launch.
+inline size_t plan_smem_bytes(const Plan &p) {
+    if (p.kind == kRowWarpKernel) return static_cast<size_t>(kRowWarps) * p.stages * p.stage_bytes;
+    return static_cast<size_t>(p.stages) * p.stage_bytes;
+}
 
 // Shared launcher: grid from occupancy, dynamic smem attribute, optional PDL.
 template <typename Kernel>
 cudaError_t launch_stream_kernel(Kernel kernel, const GemvArgs &a, const Plan &p,
                                  const DeviceInfo &dev, cudaStream_t stream) {
-    const size_t smem = static_cast<size_t>(p.stages) * p.stage_bytes + kMaxStages * sizeof(uint64_t);
+    const int threads = p.kind == kRowWarpKernel ? kRowThreads : kThreads;
+    const size_t smem = plan_smem_bytes(p);
     int per_sm = 0;
-    cudaError_t err = kernel_occupancy(reinterpret_cast<const void *>(kernel), smem, &per_sm);
+    cudaError_t err = kernel_occupancy(reinterpret_cast<const void *>(kernel), threads, smem, &per_sm);
     if (err != cudaSuccess) return err;
     if (per_sm < 1) return cudaErrorInvalidConfiguration;
     if (per_sm > p.ctas_per_sm) per_sm = p.ctas_per_sm;
+    const int64_t work_ctas = p.kind == kRowWarpKernel ? (p.n_groups + kRowWarps - 1) / kRowWarps : p.n_groups;
     int64_t grid = static_cast<int64_t>(dev.sms) * per_sm;
-    if (grid > p.n_groups) grid = p.n_groups;
+    if (grid > work_ctas) grid = work_ctas;
     if (grid > kMaxGrid) grid = kMaxGrid;
     if (grid < 1) grid = 1;
 
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(grid));
-    cfg.blockDim = dim3(kThreads);
+    cfg.blockDim = dim3(threads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];

@@ -14,7 +14,8 @@
 //     range of row groups;
 //   * a ring of shared-memory stages filled by 1-D bulk copies (TMA,
 //     cp.async.bulk) that complete on mbarriers, with L2 evict-first hints;
-//     a stage holds R whole rows of one column panel (<= 4096 columns);
+//     a stage holds R whole rows of one column panel (<= 4096 columns), and
+//     the last warp to finish reading a stage refills it at once;
 //   * each thread owns 16 columns of the panel, keeps x[0..M)[those columns]
 //     in registers pre-multiplied by the block scale, decodes its weights in
 //     registers (hardware e4m3->f16 conversion, exact) and accumulates with
@@ -24,7 +25,8 @@
 //     permutation is folded into the smem row address and the x register
 //     layout (no selects), then summed across warps in a fixed order.
 // Every output is therefore reduced in one fixed order: results are
-// deterministic and identical rows give bit-identical outputs.
+// deterministic and identical rows give bit-identical outputs.  m = 1 uses the
+// row-per-warp variant in rowwarp_gemv.cuh instead.
 #pragma once
 
 #include "device_common.cuh"
@@ -218,6 +220,56 @@ __device__ __forceinline__ void warp_argmax_merge(float &v, uint32_t &i) {
     }
 }
 
+constexpr int kAmWarps = 8;  // rows of the argmax merge scratch (one per warp)
+
+// Called by every thread of the CTA after its per-activation-row partials
+// (part_val/part_idx[blockIdx.x * M + i]) are stored.  Publishes them; the last
+// CTA to arrive merges all CTAs' partials in CTA order and writes the tokens.
+// The arrival counter wraps back to 0, ready for the next call.
+template <int M, int NT>
+__device__ __forceinline__ void argmax_cross_cta(const GemvArgs &a, float (&am_val)[kAmWarps][8],
+                                                 uint32_t (&am_idx)[kAmWarps][8], int *s_is_last) {
+    constexpr int NW = NT / 32;
+    static_assert(NW <= kAmWarps, "argmax scratch too small");
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) *s_is_last = (atomicInc(a.counter, gridDim.x - 1) == gridDim.x - 1);
+    __syncthreads();
+    if (!*s_is_last) return;
+    __threadfence();
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    for (int i = 0; i < M; ++i) {
+        float v = -INFINITY;
+        uint32_t ix = 0;
+        for (int c = threadIdx.x; c < static_cast<int>(gridDim.x); c += NT) {
+            const float cv = __ldcg(a.part_val + static_cast<int64_t>(c) * M + i);
+            const uint32_t ci = __ldcg(a.part_idx + static_cast<int64_t>(c) * M + i);
+            if (argmax_better(cv, ci, v, ix)) {
+                v = cv;
+                ix = ci;
+            }
+        }
+        warp_argmax_merge<1>(v, ix);
+        __syncthreads();
+        if (lane == 0) {
+            am_val[warp][0] = v;
+            am_idx[warp][0] = ix;
+        }
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            float bv = -INFINITY;
+            uint32_t bi = 0;
+            for (int w2 = 0; w2 < NW; ++w2)
+                if (argmax_better(am_val[w2][0], am_idx[w2][0], bv, bi)) {
+                    bv = am_val[w2][0];
+                    bi = am_idx[w2][0];
+                }
+            a.tokens[i] = bi;
+        }
+    }
+}
+
 template <int M, int FMT, bool ARGMAX>
 __global__ void __launch_bounds__(kThreads, (M <= 4 ? 2 : 1)) stream_gemv_kernel(const GemvArgs a) {
     constexpr int MP = pow2_ceil(M);
@@ -226,9 +278,11 @@ __global__ void __launch_bounds__(kThreads, (M <= 4 ? 2 : 1)) stream_gemv_kernel
     constexpr int BPW = Fmt<FMT>::kBytesPerWeight;
 
     extern __shared__ __align__(128) uint8_t smem[];
+    __shared__ __align__(8) uint64_t full[kMaxStages];
+    __shared__ unsigned int consumed[kMaxStages];
     __shared__ float red[2][kWarps][kMaxRowBatches][8];
-    __shared__ float am_val[kWarps][8];
-    __shared__ uint32_t am_idx[kWarps][8];
+    __shared__ float am_val[kAmWarps][8];
+    __shared__ uint32_t am_idx[kAmWarps][8];
     __shared__ int s_is_last;
 
     const int tid = threadIdx.x;
@@ -251,12 +305,13 @@ __global__ void __launch_bounds__(kThreads, (M <= 4 ? 2 : 1)) stream_gemv_kernel
     const int64_t n_my = g1 - g0;
     const int64_t units = n_my * a.panels;
     const int stages = a.stages;
-
     uint8_t *stage_base = smem;
-    uint64_t *full = reinterpret_cast<uint64_t *>(smem + static_cast<size_t>(stages) * a.stage_bytes);
 
     if (tid == 0) {
-        for (int s = 0; s < stages; ++s) mbar_init(smem_addr(&full[s]), 1);
+        for (int s = 0; s < stages; ++s) {
+            mbar_init(smem_addr(&full[s]), 1);
+            consumed[s] = 0;
+        }
         mbar_init_fence();
     }
     __syncthreads();
@@ -270,13 +325,11 @@ __global__ void __launch_bounds__(kThreads, (M <= 4 ? 2 : 1)) stream_gemv_kernel
     // what it reads.
     grid_dependency_wait();
     grid_launch_dependents();
-
     if (tid == 0) {
         for (int64_t u = 0; u < first; ++u)
             issue_unit<FMT>(a, u, n_my, g0, smem_addr(stage_base + u * a.stage_bytes),
                             smem_addr(&full[u]), policy, false);
     }
-    int64_t issued_end = first;
 
     float best_v = -INFINITY;
     uint32_t best_i = 0;
@@ -287,15 +340,7 @@ __global__ void __launch_bounds__(kThreads, (M <= 4 ? 2 : 1)) stream_gemv_kernel
     int64_t failed_unit = 0;
     int buf = 0;
 
-    if (units > 0) {
-        const bool to = !mbar_wait_bounded(smem_addr(&full[0]), 0);
-        if (__syncthreads_or(to)) {
-            aborted = true;
-            failed_unit = 0;
-        }
-    }
-
-    for (int64_t u = 0; u < units && !aborted; ++u) {
+    for (int64_t u = 0; u < units; ++u) {
         const int s = static_cast<int>(u % stages);
         const int panel = static_cast<int>(u / n_my);
         const int64_t row0 = (g0 + u % n_my) * a.stage_rows;
@@ -308,42 +353,48 @@ __global__ void __launch_bounds__(kThreads, (M <= 4 ? 2 : 1)) stream_gemv_kernel
             cur_panel = panel;
             cur_rblk = rblk;
         }
-        const uint8_t *st = stage_base + static_cast<size_t>(s) * a.stage_bytes;
-
-        for (int b = 0; b < rb; ++b) {
-            float p[8];
+        const bool ok = mbar_wait_bounded(smem_addr(&full[s]), static_cast<uint32_t>((u / stages) & 1));
+        if (ok) {
+            const uint8_t *st = stage_base + static_cast<size_t>(s) * a.stage_bytes;
+            for (int b = 0; b < rb; ++b) {
+                float p[8];
 #pragma unroll
-            for (int rt = 0; rt < RT; ++rt) {
-                const int lrow = team * team_rows + b * RT + (rt ^ prt);
-                float2 wv[8];
-                load_row_weights<FMT>(st + lrow * pwb, tt, team_threads, pwb, wv);
+                for (int rt = 0; rt < RT; ++rt) {
+                    const int lrow = team * team_rows + b * RT + (rt ^ prt);
+                    float2 wv[8];
+                    load_row_weights<FMT>(st + lrow * pwb, tt, team_threads, pwb, wv);
 #pragma unroll
-                for (int i = 0; i < MP; ++i) {
-                    float2 acc = make_float2(0.f, 0.f);
+                    for (int i = 0; i < MP; ++i) {
+                        float2 acc = make_float2(0.f, 0.f);
 #pragma unroll
-                    for (int k = 0; k < 8; ++k) acc = __ffma2_rn(wv[k], xr[i][k], acc);
-                    p[rt * MP + i] = acc.x + acc.y;
+                        for (int k = 0; k < 8; ++k) acc = __ffma2_rn(wv[k], xr[i][k], acc);
+                        p[rt * MP + i] = acc.x + acc.y;
+                    }
                 }
+                const float v = warp_reduce_scatter8(p);
+                if ((lane & 3) == 0) red[buf][warp][b][lane >> 2] = v;
             }
-            const float v = warp_reduce_scatter8(p);
-            if ((lane & 3) == 0) red[buf][warp][b][lane >> 2] = v;
         }
-
-        // The next stage must be full before anyone proceeds; this barrier
-        // also retires stage s and publishes red[buf].
-        bool to = false;
-        if (u + 1 < units)
-            to = !mbar_wait_bounded(smem_addr(&full[(u + 1) % stages]),
-                                     static_cast<uint32_t>(((u + 1) / stages) & 1));
-        if (__syncthreads_or(to)) {
+        // The last warp to finish reading stage s refills it, unless some
+        // warp's wait timed out (its copy may still be landing in stage s):
+        // a failed warp adds 1 to the high half of the arrival word.
+        const bool warp_ok = __all_sync(0xFFFFFFFFu, ok);
+        if (lane == 0) {
+            const unsigned int inc = warp_ok ? 1u : 0x10001u;
+            const unsigned int total = atomicAdd(&consumed[s], inc) + inc;
+            if ((total & 0xFFFFu) == kWarps) {
+                consumed[s] = 0;
+                if ((total >> 16) == 0 && u + stages < units)
+                    issue_unit<FMT>(a, u + stages, n_my, g0,
+                                    smem_addr(stage_base + static_cast<size_t>(s) * a.stage_bytes),
+                                    smem_addr(&full[s]), policy, false);
+            }
+        }
+        // Publishes red[buf]; agrees on an abort if any thread timed out.
+        if (__syncthreads_or(!ok)) {
             aborted = true;
-            failed_unit = u + 1;
-        }
-        if (!aborted && u + stages < units) {
-            if (tid == 0)
-                issue_unit<FMT>(a, u + stages, n_my, g0, smem_addr(stage_base + static_cast<size_t>(s) * a.stage_bytes),
-                                smem_addr(&full[s]), policy, false);
-            issued_end = u + stages + 1;
+            failed_unit = u;
+            break;
         }
 
         // Cross-warp sum, output write and argmax tracking.  Output slot o =
@@ -377,12 +428,13 @@ __global__ void __launch_bounds__(kThreads, (M <= 4 ? 2 : 1)) stream_gemv_kernel
     }
 
     if (aborted) {
-        // Let the copies already in flight land before the CTA's shared
-        // memory is released (each wait again bounded), then report.
+        // Units up to failed_unit + stages - 1 (and possibly the next) have
+        // been issued; let those copies land before the shared memory is
+        // released (each wait bounded), then report.
+        const int64_t issued_end = failed_unit + stages + 1 < units ? failed_unit + stages + 1 : units;
         for (int64_t u = failed_unit; u < issued_end; ++u)
             (void)mbar_wait_bounded(smem_addr(&full[u % stages]), static_cast<uint32_t>((u / stages) & 1));
         if (tid == 0) atomicOr(a.status, 1u);
-        __syncthreads();
     }
 
     if constexpr (ARGMAX) {
@@ -404,43 +456,7 @@ __global__ void __launch_bounds__(kThreads, (M <= 4 ? 2 : 1)) stream_gemv_kernel
             __stcg(a.part_val + static_cast<int64_t>(blockIdx.x) * M + tid, bv);
             __stcg(a.part_idx + static_cast<int64_t>(blockIdx.x) * M + tid, bi);
         }
-        __threadfence();
-        __syncthreads();
-        if (tid == 0) s_is_last = (atomicInc(a.counter, gridDim.x - 1) == gridDim.x - 1);
-        __syncthreads();
-        if (s_is_last) {
-            __threadfence();
-            // Merge all CTAs' partials: thread t takes CTAs t, t + 256, ...
-            for (int i = 0; i < M; ++i) {
-                float v = -INFINITY;
-                uint32_t ix = 0;
-                for (int c = tid; c < static_cast<int>(gridDim.x); c += kThreads) {
-                    const float cv = __ldcg(a.part_val + static_cast<int64_t>(c) * M + i);
-                    const uint32_t ci = __ldcg(a.part_idx + static_cast<int64_t>(c) * M + i);
-                    if (argmax_better(cv, ci, v, ix)) {
-                        v = cv;
-                        ix = ci;
-                    }
-                }
-                warp_argmax_merge<1>(v, ix);
-                __syncthreads();
-                if (lane == 0) {
-                    am_val[warp][0] = v;
-                    am_idx[warp][0] = ix;
-                }
-                __syncthreads();
-                if (tid == 0) {
-                    float bv = -INFINITY;
-                    uint32_t bi = 0;
-                    for (int w2 = 0; w2 < kWarps; ++w2)
-                        if (argmax_better(am_val[w2][0], am_idx[w2][0], bv, bi)) {
-                            bv = am_val[w2][0];
-                            bi = am_idx[w2][0];
-                        }
-                    a.tokens[i] = bi;
-                }
-            }
-        }
+        argmax_cross_cta<M, kThreads>(a, am_val, am_idx, &s_is_last);
     }
 }
 

@@ -210,13 +210,13 @@ def set_launch_tuning(target_stage_bytes: int = 0, ctas_per_sm: int = 0, use_pdl
 
 PLAN_FIELDS = ("panels", "panel_cols", "team_warps", "teams", "row_batches", "rows_per_batch",
                "stage_rows", "stage_bytes", "stages", "ctas_per_sm", "n_groups",
-               "dynamic_smem_bytes")
+               "dynamic_smem_bytes", "kernel")
 
 
 def plan_query(m: int, rows: int, cols: int, bytes_per_weight: int = 1, sms: int = 152,
                smem_per_sm: int = 233472, smem_per_block: int = 232448) -> dict:
     """Launch geometry for a shape on a device with the given facts (host only)."""
-    out = np.zeros(12, dtype=np.int64)
+    out = np.zeros(13, dtype=np.int64)
     _check(_lib.fp8blk_plan_query(m, rows, cols, bytes_per_weight, sms, smem_per_sm,
                                   smem_per_block, out.ctypes.data), "fp8blk_plan_query")
     return dict(zip(PLAN_FIELDS, (int(v) for v in out)))

@@ -8,7 +8,8 @@ import itertools
 import pytest
 
 GB300 = dict(sms=152, smem_per_sm=233472, smem_per_block=232448)
-STATIC_SMEM = 4736 + 64  # red/argmax buffers of the kernel (ptxas report) + s_is_last slack
+STATIC_SMEM = 4736 + 128  # team kernel: red/argmax buffers, barriers, counters (ptxas report)
+ROWWARP_STATIC_SMEM = 1024  # row-per-warp kernel: barriers + argmax scratch
 MAX_GRID = 1024
 
 
@@ -28,44 +29,61 @@ SHAPES = sorted(set(
          16384, 20000 - 20000 % 16))]))
 
 
+def _check_common(p, rows, cols, bpw):
+    pc, panels = p["panel_cols"], p["panels"]
+    # column panels tile [0, cols) exactly, in 16-column chunks
+    assert pc % 16 == 0 and 16 <= pc <= 4096
+    assert (panels - 1) * pc < cols <= panels * pc
+    R, sb, ns = p["stage_rows"], p["stage_bytes"], p["stages"]
+    # stage rows: a power of two dividing 128 (a group never straddles a scale row block)
+    assert R & (R - 1) == 0 and 128 % R == 0
+    # smem row reads: row < R, chunk*16 < pwb <= pc*bpw  =>  offset + 16 <= R * pc * bpw
+    assert sb == R * pc * bpw and sb % 16 == 0 and sb < (1 << 20)
+    assert 2 <= ns <= 8
+    # groups cover the rows; copies of the last group stop at `rows`
+    assert p["n_groups"] * R >= rows > (p["n_groups"] - 1) * R
+
+
+def _check_partition(n_groups, workers):
+    ends = [(b * n_groups // workers, (b + 1) * n_groups // workers) for b in range(workers)]
+    assert ends[0][0] == 0 and ends[-1][1] == n_groups
+    assert all(ends[i][1] == ends[i + 1][0] for i in range(workers - 1))
+
+
 def check_plan(ops, m, rows, cols, bpw):
     p = ops.plan_query(m, rows, cols, bpw, **GB300)
-    pc, panels, tw, teams = p["panel_cols"], p["panels"], p["team_warps"], p["teams"]
-    rb, rt, R, sb, ns = p["row_batches"], p["rows_per_batch"], p["stage_rows"], p["stage_bytes"], p["stages"]
+    _check_common(p, rows, cols, bpw)
+    pc, tw, teams = p["panel_cols"], p["team_warps"], p["teams"]
+    R, sb, ns, dyn = p["stage_rows"], p["stage_bytes"], p["stages"], p["dynamic_smem_bytes"]
+    if m == 1:
+        # row-per-warp kernel: 4 warps per CTA, each with a private ring
+        assert p["kernel"] == 1 and teams == 4 and 1 <= R <= 8
+        # a lane's chunks k*32 + lane, k < 8*bpw, cover the whole panel row
+        assert 32 * 8 * bpw * 16 >= pc * bpw
+        assert dyn == teams * ns * sb
+        assert dyn + ROWWARP_STATIC_SMEM <= GB300["smem_per_block"]
+        assert p["ctas_per_sm"] * (dyn + ROWWARP_STATIC_SMEM + 1024) <= GB300["smem_per_sm"]
+        grid = min(-(-p["n_groups"] // 4), GB300["sms"] * p["ctas_per_sm"], MAX_GRID)
+        _check_partition(p["n_groups"], grid * 4)
+        return p
+    assert p["kernel"] == 0
+    rb, rt = p["row_batches"], p["rows_per_batch"]
     mp = 1
     while mp < m:
         mp *= 2
     assert rt == 8 // mp
-    # column panels tile [0, cols) exactly, in 16-column chunks
-    assert pc % 16 == 0 and 16 <= pc <= 4096
-    assert (panels - 1) * pc < cols <= panels * pc
     # every chunk of a panel row has a thread: team_threads * 16 columns >= panel
     team_threads = tw * 32
     assert teams * tw == 8 and team_threads * 16 >= pc
-    # stage rows: a power of two dividing 128 (a group never straddles a scale row block)
-    assert R == teams * rb * rt and R & (R - 1) == 0 and 128 % R == 0
-    assert 1 <= rb <= 8
-    # smem row reads: lrow < R, chunk*16 < pwb <= pc*bpw  =>  offset + 16 <= R * pc * bpw
-    assert sb == R * pc * bpw and sb % 16 == 0 and sb < (1 << 20)
-    max_read_end = (R - 1) * pc * bpw + pc * bpw
-    assert max_read_end <= sb
+    assert R == teams * rb * rt and 1 <= rb <= 8
     # finalize: outputs per team per stage = rb * 8 slots, covered by the stride loop
     assert team_threads % 8 == 0
-    # ring depth and shared memory
-    assert 2 <= ns <= 8
-    dyn = p["dynamic_smem_bytes"]
-    assert dyn == ns * sb + 64
+    assert dyn == ns * sb
     assert dyn + STATIC_SMEM <= GB300["smem_per_block"]
     assert p["ctas_per_sm"] * (dyn + STATIC_SMEM + 1024) <= GB300["smem_per_sm"]
-    # groups cover the rows; copies of the last group stop at `rows`
-    assert p["n_groups"] * R >= rows > (p["n_groups"] - 1) * R
     grid = min(p["n_groups"], GB300["sms"] * p["ctas_per_sm"], MAX_GRID)
     assert 1 <= grid <= MAX_GRID
-    # CTA group ranges partition [0, n_groups) with no gaps
-    ng = p["n_groups"]
-    ends = [(b * ng // grid, (b + 1) * ng // grid) for b in range(grid)]
-    assert ends[0][0] == 0 and ends[-1][1] == ng
-    assert all(ends[i][1] == ends[i + 1][0] for i in range(grid - 1))
+    _check_partition(p["n_groups"], grid)
     return p
 
 
@@ -77,6 +95,6 @@ def test_plans_stay_in_bounds(ops, bpw):
 
 def test_headline_plans(ops):
     p = check_plan(ops, 1, 4096, 4096, 1)
-    assert p["panels"] == 1 and p["stage_rows"] == 8
+    assert p["panels"] == 1 and p["kernel"] == 1
     p = check_plan(ops, 8, 16384, 4096, 1)
     assert p["ctas_per_sm"] == 1
