@@ -21,7 +21,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(BUILD, "libfp8blk.so")
-SOURCES = ["abi.cu", "gemv_e4m3.cu", "gemv_bf16.cu", "nvfp4_dequant.cu"]
+SOURCES = ["abi.cu", "gemv_e4m3.cu", "gemv_bf16.cu", "nvfp4_dequant.cu", "noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

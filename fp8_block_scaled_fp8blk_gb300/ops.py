@@ -41,6 +41,9 @@ _lib.fp8blk_gemv_argmax_ws_bytes.restype = ctypes.c_size_t
 _lib.fp8blk_gemv_argmax_ws_bytes.argtypes = [_INT, _I64, _I64]
 _lib.fp8blk_gemv_argmax.restype = _INT
 _lib.fp8blk_gemv_argmax.argtypes = [_P, _P, _P, _P, _P, _P, ctypes.c_size_t, _INT, _I64, _I64, _P]
+_lib.fp8blk_gemv_argmax_noalloc.restype = _INT
+_lib.fp8blk_gemv_argmax_noalloc.argtypes = [_P, _P, _P, _P, _P, _INT, _I64, _I64, _P]
+_lib.fp8blk_noalloc_scratch_bytes.restype = ctypes.c_size_t
 _lib.fp8blk_bf16_gemv.restype = _INT
 _lib.fp8blk_bf16_gemv.argtypes = [_P, _P, _P, _INT, _I64, _I64, _P]
 _lib.nvfp4_expert_dequant.restype = _INT
@@ -142,6 +145,24 @@ def fp8blk_gemv_argmax(w_codes: torch.Tensor, scales: torch.Tensor, x: torch.Ten
     _check(_lib.fp8blk_gemv_argmax(_ptr(w_codes), _ptr(scales), _ptr(x2), _ptr(logits),
                                    _ptr(tokens), _ptr(ws), ws.numel() * ws.element_size(), m,
                                    rows, cols, _stream(x)), "fp8blk_gemv_argmax")
+    return tokens
+
+
+def fp8blk_gemv_argmax_noalloc(w_codes: torch.Tensor, scales: torch.Tensor, x: torch.Tensor,
+                               tokens: torch.Tensor | None = None,
+                               logits: torch.Tensor | None = None) -> torch.Tensor:
+    """fp8blk_gemv_argmax with the library's own fixed device scratch (no workspace).
+
+    For callers that cannot allocate device memory; calls must not overlap on the GPU.
+    """
+    rows, cols = w_codes.shape
+    x2 = x if x.dim() == 2 else x.view(1, -1)
+    m = x2.shape[0]
+    if tokens is None:
+        tokens = torch.empty(m, dtype=torch.int32, device=x.device)
+    _check(_lib.fp8blk_gemv_argmax_noalloc(_ptr(w_codes), _ptr(scales), _ptr(x2), _ptr(logits),
+                                           _ptr(tokens), m, rows, cols, _stream(x)),
+           "fp8blk_gemv_argmax_noalloc")
     return tokens
 
 

@@ -116,6 +116,38 @@ int fp8blk_gemv_argmax(const uint8_t *w_codes, const float *scales, const float 
                        int64_t rows, int64_t cols, void *stream);
 
 /*
+ * fp8blk_gemv_argmax_noalloc -- fp8blk_gemv_argmax for callers that cannot
+ * allocate device memory.  No counterpart in the paper: the pages' engine
+ * preallocates its own arenas.  This entry point serves callers that cannot
+ * hand the library a workspace: code running while a CUDA graph is being
+ * captured (no cudaMalloc then), serving loops that must not call
+ * cudaMalloc/cudaFree because those synchronize the device, and plain C hosts
+ * or plugins that own no allocator.  It computes exactly what
+ * fp8blk_gemv_argmax computes, with the workspace placed in a fixed array of
+ * fp8blk_noalloc_scratch_bytes() bytes (64.25 KiB) in the library's own device
+ * memory; every GPU that loads the library holds that array until the process
+ * exits.  It allocates nothing, and calls no cudaMalloc or cudaFree.
+ *   Arguments as fp8blk_gemv_argmax, without ws / ws_bytes.
+ *   Size limit: the workspace fp8blk_gemv_argmax_ws_bytes(m, rows, cols) must
+ *   fit in the array -- any m <= 8 with cols <= 4096; wider rows only for
+ *   tiny rows x m.  Larger shapes return FP8BLK_ERANGE.
+ *   Set-up: the first call on each device looks up the array's device address
+ *   (cudaGetSymbolAddress) with that device current; make that first call
+ *   before any stream capture.
+ *   Sharing: every call uses the same array, which keeps the last call's
+ *   contents; each call clears the part that must start at zero with a
+ *   stream-ordered memset.  Calls whose GPU work overlaps (different streams,
+ *   or different host threads) race on the array: serialize them.
+ * Errors: as fp8blk_gemv_argmax, with ERANGE in place of EWS.
+ */
+int fp8blk_gemv_argmax_noalloc(const uint8_t *w_codes, const float *scales, const float *x,
+                               float *logits, uint32_t *tokens, int m, int64_t rows, int64_t cols,
+                               void *stream);
+
+/* Size in bytes of the fixed device array fp8blk_gemv_argmax_noalloc uses. */
+size_t fp8blk_noalloc_scratch_bytes(void);
+
+/*
  * fp8blk_bf16_gemv -- y[i][r] = sum_c bf16(B[r][c]) * x[i][c], f32
  * accumulation.  The GEMV that follows the per-expert dequant.  Source:
  * "Module dsv4_gpu" page, module header (bf16 GEMMs with f32 accumulation)
