@@ -58,9 +58,16 @@ def nvfp4_bytes(n_active: int, rows: int, cols: int) -> int:
     return n_active * per + cols * 4 + n_active * rows * 4
 
 
+# Sources that define the streaming kernels and their launch geometry.
+KERNEL_SOURCES = ("device_common.cuh", "stream_gemv.cuh", "rowwarp_gemv.cuh", "launch.h", "abi.cu",
+                  "gemv_e4m3.cu", "gemv_bf16.cu", "nvfp4_dequant.cu")
+
+
 def source_hash() -> str:
+    """Hash of the kernel sources; a committed ncu traffic figure is reported
+    only while it matches (i.e. while the kernels are the ones profiled)."""
     h = hashlib.sha1()
-    for name in sorted(os.listdir(CSRC)):
+    for name in KERNEL_SOURCES:
         with open(os.path.join(CSRC, name), "rb") as f:
             h.update(name.encode())
             h.update(f.read())
@@ -167,13 +174,22 @@ def dist_setup():
 
 
 def max_over_ranks(value: float, world: int, device) -> float:
+    """Slowest rank's value (all ranks get it).  Timing only: not a data path."""
     if world == 1:
         return value
     import torch
     import torch.distributed as dist
+    if dist.get_backend() == "gloo":
+        device = "cpu"
     t = torch.tensor([value], dtype=torch.float64, device=device)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def replica_throughput(bytes_per_call: int, us_per_call_slowest: float, world: int) -> float:
+    """Whole-job GB/s of `world` independent replicas, each doing the same calls,
+    timed by the slowest rank."""
+    return world * bytes_per_call / (us_per_call_slowest * 1e-6) / 1e9
 
 
 def barrier(world: int):
@@ -396,7 +412,7 @@ def run_ours(args):
         sampler.stop()
     us = ms * 1e3 / args.steps
     per_gpu_gbs = st["bytes"] / (us * 1e-6) / 1e9
-    value = world * per_gpu_gbs
+    value = replica_throughput(st["bytes"], us, world)
     status = ops.fp8blk_device_status()
     e2e = measure_e2e(st, args.steps, device)
     e2e["value"] = round(e2e["value"] * world, 2) if world > 1 else e2e["value"]
@@ -422,7 +438,7 @@ def run_ours(args):
                        "parallelism": f"replicas x{world}"},
             "roofline": {"bound": "hbm", "achieved": round(per_gpu_gbs, 1), "peak": peak, "unit": "GB/s",
                          "frac": round(per_gpu_gbs / peak, 4), "traffic": profiled_traffic(HEADLINE),
-                         "peak_source": peak_src, "kernel": "stream_gemv_kernel<1,e4m3,false>",
+                         "peak_source": peak_src, "kernel": "rowwarp_gemv_kernel<e4m3,false> (m = 1)",
                          "algorithmic_bytes_per_launch": st["bytes"]},
             "e2e": e2e,
             "gpu_launches": args.steps,
@@ -501,6 +517,23 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+def run_profile_workload(args):
+    """Just `--calls` calls of one named workload, for an ncu capture."""
+    import torch
+    from fp8_block_scaled_fp8blk_gb300 import ops
+    device = torch.device("cuda", 0)
+    torch.cuda.set_device(device)
+    if args.profile_workload == "nvfp4_experts_6of64_2048x4096":
+        st = setup_nvfp4(device)
+    else:
+        st = setup_fp8blk(args.profile_workload, device, args.profile_workload.startswith("head_argmax"))
+    for i in range(args.calls):
+        st["calls"][i % len(st["calls"])]()
+    torch.cuda.synchronize()
+    print(json.dumps({"profile_workload": args.profile_workload, "calls": args.calls,
+                      "device_status": ops.fp8blk_device_status()}))
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -509,7 +542,13 @@ def main():
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--no-extra", action="store_true", help="skip the other workloads")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--profile-workload", default=None,
+                    help="run --calls calls of this workload and exit (for ncu captures)")
+    ap.add_argument("--calls", type=int, default=6)
     args = ap.parse_args()
+    if args.profile_workload:
+        run_profile_workload(args)
+        return
     if args.warmup < 3:
         args.warmup = 3
     if args.impl == "reference":

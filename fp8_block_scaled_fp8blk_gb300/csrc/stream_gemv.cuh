@@ -19,7 +19,7 @@
 //   * each thread owns 16 columns of the panel, keeps x[0..M)[those columns]
 //     in registers pre-multiplied by the block scale, decodes its weights in
 //     registers (hardware e4m3->f16 conversion, exact) and accumulates with
-//     packed f32x2 FMAs;
+//     scalar FMAs (measured faster than packed f32x2 FMAs here);
 //   * the 8 per-lane partials (RT rows x MP activation rows) are reduced
 //     across the warp by a 3-level reduce-scatter whose lane-dependent slot
 //     permutation is folded into the smem row address and the x register
@@ -134,12 +134,13 @@ __device__ __forceinline__ void issue_unit(const GemvArgs &a, int64_t u, int64_t
 }
 
 // Decode this thread's 16 columns of one staged row into 8 f32 pairs.
-// Chunks past the panel edge read nothing and decode to zero.
-template <int FMT>
+// Chunks past the panel edge read nothing and decode to zero; FULL: the panel
+// is a whole kMaxPanelCols wide, so no chunk is past the edge.
+template <int FMT, bool FULL>
 __device__ __forceinline__ void load_row_weights(const uint8_t *row, int tt, int team_threads,
                                                  int pwb, float2 wv[8]) {
     if constexpr (FMT == kE4M3) {
-        if (tt * 16 < pwb) {
+        if (FULL || tt * 16 < pwb) {
             const uint4 q = *reinterpret_cast<const uint4 *>(row + tt * 16);
             e4m3x4_to_f32(q.x, wv[0], wv[1]);
             e4m3x4_to_f32(q.y, wv[2], wv[3]);
@@ -153,7 +154,7 @@ __device__ __forceinline__ void load_row_weights(const uint8_t *row, int tt, int
 #pragma unroll
         for (int s = 0; s < 2; ++s) {
             const int chunk = s * team_threads + tt;
-            if (chunk * 16 < pwb) {
+            if (FULL || chunk * 16 < pwb) {
                 const uint4 q = *reinterpret_cast<const uint4 *>(row + chunk * 16);
                 wv[4 * s + 0] = bf16x2_to_f32(q.x);
                 wv[4 * s + 1] = bf16x2_to_f32(q.y);
@@ -164,6 +165,57 @@ __device__ __forceinline__ void load_row_weights(const uint8_t *row, int tt, int
                 for (int k = 0; k < 4; ++k) wv[4 * s + k] = make_float2(0.f, 0.f);
             }
         }
+    }
+}
+
+// All row batches of one staged unit: per lane, per batch, 8 partial sums
+// (RT rows x MP activation rows), reduced across the warp into red_w[b][*].
+// Scalar FMAs, two independent chains per (row, activation row).
+template <int M, int FMT, bool FULL>
+__device__ __forceinline__ void team_stage_compute(const uint8_t *st, int pwb, int rb, int team,
+                                                   int team_rows, int tt, int team_threads, int prt,
+                                                   int lane, const float2 (&xr)[pow2_ceil(M)][8],
+                                                   float (*red_w)[8]) {
+    constexpr int MP = pow2_ceil(M);
+    constexpr int RT = 8 / MP;
+    // Partial sums of one row batch: 8 slots (RT rows x MP activation rows).
+    auto batch_partials = [&](int b, float (&p)[8]) {
+#pragma unroll
+        for (int rt = 0; rt < RT; ++rt) {
+            const int lrow = team * team_rows + b * RT + (rt ^ prt);
+            float2 wv[8];
+            load_row_weights<FMT, FULL>(st + lrow * pwb, tt, team_threads, pwb, wv);
+#pragma unroll
+            for (int i = 0; i < MP; ++i) {
+                float a0 = 0.f, a1 = 0.f;
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    a0 = fmaf(wv[k].x, xr[i][k].x, a0);
+                    a1 = fmaf(wv[k].y, xr[i][k].y, a1);
+                }
+                p[rt * MP + i] = a0 + a1;
+            }
+        }
+    };
+    // Two batches per step, so that one batch's shuffle chain can overlap the
+    // other's arithmetic.
+    int b = 0;
+    for (; b + 1 < rb; b += 2) {
+        float p0[8], p1[8];
+        batch_partials(b, p0);
+        batch_partials(b + 1, p1);
+        const float v0 = warp_reduce_scatter8(p0);
+        const float v1 = warp_reduce_scatter8(p1);
+        if ((lane & 3) == 0) {
+            red_w[b][lane >> 2] = v0;
+            red_w[b + 1][lane >> 2] = v1;
+        }
+    }
+    if (b < rb) {
+        float p0[8];
+        batch_partials(b, p0);
+        const float v0 = warp_reduce_scatter8(p0);
+        if ((lane & 3) == 0) red_w[b][lane >> 2] = v0;
     }
 }
 
@@ -356,24 +408,12 @@ __global__ void __launch_bounds__(kThreads, (M <= 4 ? 2 : 1)) stream_gemv_kernel
         const bool ok = mbar_wait_bounded(smem_addr(&full[s]), static_cast<uint32_t>((u / stages) & 1));
         if (ok) {
             const uint8_t *st = stage_base + static_cast<size_t>(s) * a.stage_bytes;
-            for (int b = 0; b < rb; ++b) {
-                float p[8];
-#pragma unroll
-                for (int rt = 0; rt < RT; ++rt) {
-                    const int lrow = team * team_rows + b * RT + (rt ^ prt);
-                    float2 wv[8];
-                    load_row_weights<FMT>(st + lrow * pwb, tt, team_threads, pwb, wv);
-#pragma unroll
-                    for (int i = 0; i < MP; ++i) {
-                        float2 acc = make_float2(0.f, 0.f);
-#pragma unroll
-                        for (int k = 0; k < 8; ++k) acc = __ffma2_rn(wv[k], xr[i][k], acc);
-                        p[rt * MP + i] = acc.x + acc.y;
-                    }
-                }
-                const float v = warp_reduce_scatter8(p);
-                if ((lane & 3) == 0) red[buf][warp][b][lane >> 2] = v;
-            }
+            if (pwb == kMaxPanelCols * BPW)
+                team_stage_compute<M, FMT, true>(st, pwb, rb, team, team_rows, tt, team_threads, prt, lane,
+                                                 xr, red[buf][warp]);
+            else
+                team_stage_compute<M, FMT, false>(st, pwb, rb, team, team_rows, tt, team_threads, prt, lane,
+                                                  xr, red[buf][warp]);
         }
         // The last warp to finish reading stage s refills it, unless some
         // warp's wait timed out (its copy may still be landing in stage s):
