@@ -95,7 +95,10 @@ Plan make_plan(int m, int64_t rows, int64_t cols, int bpw, const DeviceInfo &dev
     const int64_t per = (cols + panels0 - 1) / panels0;
     p.panel_cols = static_cast<int>((per + 15) / 16 * 16);
     p.panels = static_cast<int>((cols + p.panel_cols - 1) / p.panel_cols);
-    if (m == 1) {
+    const bool use_rowwarp =
+        m == 1 && (t.m1_kernel == 1 ||
+                   (t.m1_kernel == 0 && rows * cols * bpw >= t.m1_rowwarp_min_bytes));
+    if (use_rowwarp) {
         // Row-per-warp kernel: each warp streams whole panel rows through a
         // private ring; stages of about target/4 bytes, shrunk while there
         // are fewer row groups than warps.
@@ -406,6 +409,13 @@ int fp8blk_set_launch_tuning(int target_stage_bytes, int ctas_per_sm, int use_pd
     t.use_pdl = use_pdl != 0;
     t.l2_prefetch = l2_prefetch != 0;
     t.max_stages = max_stages ? max_stages : kMaxStages;
+    return FP8BLK_OK;
+}
+
+int fp8blk_set_m1_kernel(int choice, int64_t rowwarp_min_bytes) {
+    if (choice < 0 || choice > 2 || rowwarp_min_bytes < 0) return FP8BLK_EINVAL;
+    tuning().m1_kernel = choice;
+    tuning().m1_rowwarp_min_bytes = rowwarp_min_bytes ? rowwarp_min_bytes : (96ll << 20);
     return FP8BLK_OK;
 }
 

@@ -18,6 +18,7 @@ cudaError_t launch_gemv_e4m3(const GemvArgs &a, const Plan &p, int m, bool argma
         return launch_stream_kernel(rowwarp_gemv_kernel<kE4M3, false>, a, p, dev, stream);
     }
     switch (m) {
+        case 1: return launch_m<1>(a, p, argmax, dev, stream);
         case 2: return launch_m<2>(a, p, argmax, dev, stream);
         case 3: return launch_m<3>(a, p, argmax, dev, stream);
         case 4: return launch_m<4>(a, p, argmax, dev, stream);

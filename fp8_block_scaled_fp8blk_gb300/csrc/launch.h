@@ -19,6 +19,8 @@ struct Tuning {
     int use_pdl = 1;                     // programmatic dependent launch
     int l2_prefetch = 1;                 // L2 prefetch of the first stages before the PDL wait
     int max_stages = kMaxStages;
+    int m1_kernel = 0;                   // m = 1: 0 = by size, 1 = row-per-warp, 2 = team
+    int64_t m1_rowwarp_min_bytes = 96ll << 20;  // by size: row-per-warp from this many weight bytes
 };
 Tuning &tuning();
 

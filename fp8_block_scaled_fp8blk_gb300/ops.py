@@ -52,6 +52,8 @@ _lib.nvfp4_expert_dequant_gemv.restype = _INT
 _lib.nvfp4_expert_dequant_gemv.argtypes = [_P, _P, _P, _INT, _P, _INT, _P, _P, _P, _I64, _I64, _P]
 _lib.fp8blk_set_launch_tuning.restype = _INT
 _lib.fp8blk_set_launch_tuning.argtypes = [_INT, _INT, _INT, _INT, _INT]
+_lib.fp8blk_set_m1_kernel.restype = _INT
+_lib.fp8blk_set_m1_kernel.argtypes = [_INT, _I64]
 _lib.fp8blk_plan_query.restype = _INT
 _lib.fp8blk_plan_query.argtypes = [_INT, _I64, _I64, _INT, _INT, _INT, _INT, _P]
 _lib.fp8blk_device_status.restype = _INT
@@ -241,6 +243,11 @@ def plan_query(m: int, rows: int, cols: int, bytes_per_weight: int = 1, sms: int
     _check(_lib.fp8blk_plan_query(m, rows, cols, bytes_per_weight, sms, smem_per_sm,
                                   smem_per_block, out.ctypes.data), "fp8blk_plan_query")
     return dict(zip(PLAN_FIELDS, (int(v) for v in out)))
+
+
+def set_m1_kernel(choice: int = 0, rowwarp_min_bytes: int = 0) -> None:
+    """m = 1 kernel: 0 by size, 1 row-per-warp, 2 team (speed only)."""
+    _check(_lib.fp8blk_set_m1_kernel(choice, rowwarp_min_bytes), "fp8blk_set_m1_kernel")
 
 
 def fp8blk_device_status(clear: bool = False) -> int:

@@ -216,15 +216,24 @@ int fp8blk_set_launch_tuning(int target_stage_bytes, int ctas_per_sm, int use_pd
                              int max_stages);
 
 /*
+ * fp8blk_set_m1_kernel -- which kernel serves m = 1 (speed only; results are
+ * identical to within the stated error bound, and bit-identical run to run):
+ *   choice 0 = by size (row-per-warp when rows * cols * bytes_per_weight >=
+ *   rowwarp_min_bytes, 0 = default 96 MiB; the team kernel below), 1 = always
+ *   row-per-warp, 2 = always the team kernel.  Errors: EINVAL.
+ */
+int fp8blk_set_m1_kernel(int choice, int64_t rowwarp_min_bytes);
+
+/*
  * fp8blk_plan_query -- HOST, no CUDA calls: the launch geometry the streaming
  * GEMV would use for this shape on a device with the given SM count and
  * shared-memory limits (bytes), for inspection and bounds checks.
  *   bytes_per_weight  1 (e4m3) or 2 (bf16)
  *   out  host int64[13]: panels, panel_cols, team_warps, teams, row_batches,
  *        rows_per_batch, stage_rows, stage_bytes, stages, ctas_per_sm,
- *        n_groups, dynamic_smem_bytes, kernel (0 = team kernel for m >= 2,
- *        1 = row-per-warp kernel for m = 1; for kernel 1, stage_bytes and
- *        stages describe each warp's private ring and teams = warps per CTA)
+ *        n_groups, dynamic_smem_bytes, kernel (0 = team kernel, 1 = row-per-warp
+ *        kernel (m = 1, large matrices); for kernel 1, stage_bytes and stages
+ *        describe each warp's private ring and teams = warps per CTA)
  * Errors: EINVAL (bad shape or device facts).
  */
 int fp8blk_plan_query(int m, int64_t rows, int64_t cols, int bytes_per_weight, int sms,

@@ -154,3 +154,34 @@ def test_bf16_gemv_matches_oracle(ops):
 
 def test_device_status_clean(ops):
     assert ops.fp8blk_device_status() == 0
+
+
+@pytest.mark.parametrize("choice", [1, 2])
+def test_m1_both_kernels_match_oracle(ops, choice):
+    """m = 1 is served by the row-per-warp kernel (large) or the team kernel
+    (small); force each on ragged and multi-panel shapes, plain and argmax."""
+    ops.set_m1_kernel(choice)
+    try:
+        for rows, cols in [(1, 16), (130, 272), (1000, 1040), (4097, 4096), (77, 8208), (300, 12304)]:
+            case = synth.fp8blk_case(rows, cols, 1, seed=rows * 7 + cols + choice)
+            y = run_gemv(ops, case)
+            ref, a = oracle.fp8blk_gemv(case.codes, case.scale_e8m0, case.x, nthreads=8)
+            assert_close(y, ref, a, f"m1 kernel {choice} {rows}x{cols}")
+            w, s, x = to_dev(case.codes), scales_dev(case.scale_e8m0), to_dev(case.x)
+            ws = ops.argmax_workspace(1, rows, cols, "cuda:0")
+            logits = torch.empty((1, rows), dtype=torch.float32, device="cuda:0")
+            tok = ops.fp8blk_gemv_argmax(w, s, x, ws, logits=logits).cpu().numpy().view(np.uint32)
+            lg = logits.cpu().numpy()
+            assert_close(lg, ref, a, f"m1 argmax logits {choice} {rows}x{cols}")
+            assert tok[0] == oracle.argmax(lg[0].astype(np.float64))
+        rng = np.random.default_rng(40 + choice)
+        for rows, cols in [(2048, 4096), (131, 272), (70, 8208)]:
+            sign = rng.integers(0, 2, size=(rows, cols), dtype=np.uint16) << 15
+            expo = rng.integers(110, 141, size=(rows, cols), dtype=np.uint16) << 7
+            b = sign | expo | rng.integers(0, 128, size=(rows, cols), dtype=np.uint16)
+            x = rng.standard_normal((1, cols)).astype(np.float32)
+            yb = ops.fp8blk_bf16_gemv(to_dev(b.view(np.int16)), to_dev(x)).cpu().numpy()
+            ref, a = oracle.bf16_gemv(b, x, nthreads=8)
+            assert_close(yb, ref, a, f"m1 bf16 kernel {choice} {rows}x{cols}")
+    finally:
+        ops.set_m1_kernel(0)

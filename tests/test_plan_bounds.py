@@ -55,9 +55,9 @@ def check_plan(ops, m, rows, cols, bpw):
     _check_common(p, rows, cols, bpw)
     pc, tw, teams = p["panel_cols"], p["team_warps"], p["teams"]
     R, sb, ns, dyn = p["stage_rows"], p["stage_bytes"], p["stages"], p["dynamic_smem_bytes"]
-    if m == 1:
+    if p["kernel"] == 1:
         # row-per-warp kernel: 4 warps per CTA, each with a private ring
-        assert p["kernel"] == 1 and teams == 4 and 1 <= R <= 8
+        assert m == 1 and teams == 4 and 1 <= R <= 8
         # a lane's chunks k*32 + lane, k < 8*bpw, cover the whole panel row
         assert 32 * 8 * bpw * 16 >= pc * bpw
         assert dyn == teams * ns * sb
@@ -88,13 +88,20 @@ def check_plan(ops, m, rows, cols, bpw):
 
 
 @pytest.mark.parametrize("bpw", [1, 2])
-def test_plans_stay_in_bounds(ops, bpw):
-    for m, rows, cols in SHAPES:
-        check_plan(ops, m, rows, cols, bpw)
+@pytest.mark.parametrize("m1_kernel", [1, 2])
+def test_plans_stay_in_bounds(ops, bpw, m1_kernel):
+    ops.set_m1_kernel(m1_kernel)
+    try:
+        for m, rows, cols in SHAPES:
+            check_plan(ops, m, rows, cols, bpw)
+    finally:
+        ops.set_m1_kernel(0)
 
 
 def test_headline_plans(ops):
     p = check_plan(ops, 1, 4096, 4096, 1)
-    assert p["panels"] == 1 and p["kernel"] == 1
+    assert p["panels"] == 1 and p["kernel"] == 0  # small: team kernel
+    p = check_plan(ops, 1, 131072, 4096, 1)
+    assert p["kernel"] == 1  # large: row-per-warp
     p = check_plan(ops, 8, 16384, 4096, 1)
     assert p["ctas_per_sm"] == 1
