@@ -45,6 +45,19 @@ CSRC = os.path.join(ROOT, "fp8_block_scaled_fp8blk_gb300", "csrc")
 
 
 # ---------------------------------------------------------------- byte counts
+KERNEL_NAMES = {0: "stream_gemv_kernel<{m},e4m3,{a}> (team kernel)",
+                1: "rowwarp_gemv_kernel<e4m3,{a}> (row-per-warp kernel)",
+                2: "tc_gemv_kernel<{a}> (tensor-core kernel)"}
+
+
+def kernel_name(ops, m: int, rows: int, cols: int, argmax: bool = False) -> str:
+    """The kernel the library's planner picks for this shape on this device."""
+    import torch
+    prop = torch.cuda.get_device_properties(torch.cuda.current_device())
+    kind = ops.plan_query(m, rows, cols, 1, sms=prop.multi_processor_count)["kernel"]
+    return KERNEL_NAMES[kind].format(m=m, a=str(argmax).lower())
+
+
 def fp8blk_bytes(rows: int, cols: int, m: int, argmax: bool = False) -> int:
     """codes + f32 scale grid + activations + outputs (tokens for argmax)."""
     grid = math.ceil(rows / 128) * math.ceil(cols / 128) * 4
@@ -307,6 +320,7 @@ def setup_nvfp4(device):
 
 def measure_extra(device, stream, world, peak):
     """The other workloads of the path, measured the same way (one JSON line)."""
+    from fp8_block_scaled_fp8blk_gb300 import ops
     out = {}
     for name, argmax, steps in (("gemv_512x1024_m1", False, 4000),
                                 ("head_argmax_131072x4096_m1", True, 300),
@@ -318,7 +332,8 @@ def measure_extra(device, stream, world, peak):
         gbs = st["bytes"] / (us * 1e-6) / 1e9
         out[name] = {"us_per_call": round(us, 3), "gbs": round(gbs, 1),
                      "frac_of_hbm_peak": round(gbs / peak, 4), "bytes_per_call": st["bytes"],
-                     "weight_copies": st["copies"], "steps": steps}
+                     "weight_copies": st["copies"], "steps": steps,
+                     "kernel": kernel_name(ops, st["m"], st["rows"], st["cols"], argmax)}
         del st
     st = setup_nvfp4(device)
     steps = 500
@@ -396,6 +411,7 @@ def run_ours(args):
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=device)
     from fp8_block_scaled_fp8blk_gb300 import ops
+    ops.set_tensor_core_min_m(args.tensor_core_min_m, args.tensor_core_min_bytes)
     peak, peak_src = hbm_peak()
     stream = torch.cuda.Stream(device)
     st = setup_fp8blk(HEADLINE, device)
@@ -438,7 +454,8 @@ def run_ours(args):
                        "parallelism": f"replicas x{world}"},
             "roofline": {"bound": "hbm", "achieved": round(per_gpu_gbs, 1), "peak": peak, "unit": "GB/s",
                          "frac": round(per_gpu_gbs / peak, 4), "traffic": profiled_traffic(HEADLINE),
-                         "peak_source": peak_src, "kernel": "rowwarp_gemv_kernel<e4m3,false> (m = 1)",
+                         "peak_source": peak_src,
+                         "kernel": kernel_name(ops, st["m"], st["rows"], st["cols"]),
                          "algorithmic_bytes_per_launch": st["bytes"]},
             "e2e": e2e,
             "gpu_launches": args.steps,
@@ -523,6 +540,7 @@ def run_profile_workload(args):
     from fp8_block_scaled_fp8blk_gb300 import ops
     device = torch.device("cuda", 0)
     torch.cuda.set_device(device)
+    ops.set_tensor_core_min_m(args.tensor_core_min_m, args.tensor_core_min_bytes)
     if args.profile_workload == "nvfp4_experts_6of64_2048x4096":
         st = setup_nvfp4(device)
     else:
@@ -545,6 +563,10 @@ def main():
     ap.add_argument("--profile-workload", default=None,
                     help="run --calls calls of this workload and exit (for ncu captures)")
     ap.add_argument("--calls", type=int, default=6)
+    ap.add_argument("--tensor-core-min-m", type=int, default=0,
+                    help="e4m3 GEMVs with m >= this use the tensor-core kernel (9 = never, 0 = library default)")
+    ap.add_argument("--tensor-core-min-bytes", type=int, default=0,
+                    help="... when the weights are at least this many bytes (1 = any, 0 = library default)")
     args = ap.parse_args()
     if args.profile_workload:
         run_profile_workload(args)

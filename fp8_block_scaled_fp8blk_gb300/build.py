@@ -4,6 +4,9 @@ Compiles the translation units in ``csrc/`` in parallel and links them into
 ``_build/libfp8blk.so`` (shared CUDA runtime, so the library shares torch's
 runtime and streams).  Rebuilds only when a source or header is newer than the
 library.  Usage: ``python -m fp8_block_scaled_fp8blk_gb300.build [--force] [-v]``.
+Extra nvcc flags (e.g. ``-DTC_E_STAGES=6`` for the tensor-core kernel's ring
+depths) come from the ``FP8BLK_NVCC_EXTRA`` environment variable; changing
+them needs ``--force``.
 """
 from __future__ import annotations
 
@@ -21,7 +24,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(BUILD, "libfp8blk.so")
-SOURCES = ["abi.cu", "gemv_e4m3.cu", "gemv_bf16.cu", "nvfp4_dequant.cu", "noalloc.cu"]
+SOURCES = ["abi.cu", "gemv_e4m3.cu", "gemv_bf16.cu", "gemv_tc.cu", "nvfp4_dequant.cu", "noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
@@ -34,7 +37,7 @@ def _nvcc() -> str:
 
 def _flags(ptxas_verbose: bool) -> list[str]:
     f = ["-std=c++17", "-O3", "-lineinfo", *ARCH, "-Xcompiler", "-fPIC,-O2",
-         "-I", INCLUDE, "-I", CSRC]
+         "-I", INCLUDE, "-I", CSRC, *os.environ.get("FP8BLK_NVCC_EXTRA", "").split()]
     if ptxas_verbose:
         f += ["-Xptxas", "-v"]
     return f

@@ -79,6 +79,74 @@ cudaError_t kernel_occupancy(const void *kernel, int threads, size_t smem, int *
     return cudaSuccess;
 }
 
+namespace {
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                  const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+}  // namespace
+
+static EncodeTiledFn encode_tiled_fn(cudaError_t *err) {
+    static EncodeTiledFn fn = nullptr;
+    if (!fn) {
+        void *f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        *err = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q);
+        if (*err == cudaSuccess && (!f || q != cudaDriverEntryPointSuccess)) *err = cudaErrorNotSupported;
+        if (*err != cudaSuccess) return nullptr;
+        fn = reinterpret_cast<EncodeTiledFn>(f);
+    }
+    *err = cudaSuccess;
+    return fn;
+}
+
+namespace {
+struct MapEntry {
+    const void *ptr;
+    int64_t rows, cols;
+    int box_rows, box_cols, dtype;
+    CUtensorMap map;
+};
+std::mutex g_map_mu;
+MapEntry g_maps[128];
+int g_map_next = 0;
+
+// Encodes (or finds) a 2-D tensor map of a rows x cols row-major array.
+cudaError_t tensor_map_2d(const void *ptr, int64_t rows, int64_t cols, int elem_bytes, CUtensorMapDataType dtype,
+                          int box_rows, int box_cols, CUtensorMapSwizzle swizzle, CUtensorMap *out) {
+    std::lock_guard<std::mutex> lock(g_map_mu);
+    for (const MapEntry &e : g_maps)
+        if (e.ptr == ptr && e.rows == rows && e.cols == cols && e.box_rows == box_rows && e.box_cols == box_cols &&
+            e.dtype == static_cast<int>(dtype)) {
+            *out = e.map;
+            return cudaSuccess;
+        }
+    cudaError_t err;
+    EncodeTiledFn fn = encode_tiled_fn(&err);
+    if (!fn) return err;
+    CUtensorMap map;
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * elem_bytes};
+    const cuuint32_t box[2] = {static_cast<cuuint32_t>(box_cols), static_cast<cuuint32_t>(box_rows)};
+    const cuuint32_t estr[2] = {1u, 1u};
+    const CUresult r = fn(&map, dtype, 2, const_cast<void *>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+    g_maps[g_map_next] = MapEntry{ptr, rows, cols, box_rows, box_cols, static_cast<int>(dtype), map};
+    g_map_next = (g_map_next + 1) % 128;
+    *out = map;
+    return cudaSuccess;
+}
+}  // namespace
+
+cudaError_t weight_tensor_map(const uint8_t *w, int64_t rows, int64_t cols, int box_rows, CUtensorMap *out) {
+    return tensor_map_2d(w, rows, cols, 1, CU_TENSOR_MAP_DATA_TYPE_UINT8, box_rows, kTcKb, CU_TENSOR_MAP_SWIZZLE_128B,
+                         out);
+}
+
+cudaError_t activation_tensor_map(const float *x, int m, int64_t cols, int box_cols, CUtensorMap *out) {
+    return tensor_map_2d(x, m, cols, 4, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, m, box_cols, CU_TENSOR_MAP_SWIZZLE_NONE, out);
+}
+
 static int pow2_floor(int v) {
     int p = 1;
     while (2 * p <= v) p *= 2;
@@ -95,6 +163,25 @@ Plan make_plan(int m, int64_t rows, int64_t cols, int bpw, const DeviceInfo &dev
     const int64_t per = (cols + panels0 - 1) / panels0;
     p.panel_cols = static_cast<int>((per + 15) / 16 * 16);
     p.panels = static_cast<int>((cols + p.panel_cols - 1) / p.panel_cols);
+    const int64_t tc_units8 = (rows + 7) / 8;
+    const int64_t tc_rows_per_cta = (tc_units8 + dev.sms - 1) / dev.sms * 8;
+    const int64_t tc_row_blocks = tc_rows_per_cta / 128 + 2;  // most a CTA can span
+    if (bpw == 1 && m >= 2 && t.tc_min_m >= 2 && m >= t.tc_min_m && cols >= kTcKb && rows * cols >= t.tc_min_bytes &&
+        tc_row_blocks <= kTcMaxRowBlocks && tc_row_blocks * ((cols + 127) / 128) <= kTcMaxSf) {
+        // Tensor-core kernel: one CTA per SM, whole 8-row units per CTA,
+        // column panels of at most kTcMaxPanel (a multiple of kTcKb).
+        p.kind = kTensorCoreKernel;
+        p.panels = static_cast<int>((cols + kTcMaxPanel - 1) / kTcMaxPanel);
+        p.panel_cols = p.panels == 1 ? static_cast<int>(cols) : kTcMaxPanel;
+        p.team_warps_log2 = 0;
+        p.rb = 1;
+        p.stage_rows = kTcM;
+        p.stage_bytes = kTcETileBytes;
+        p.stages = kTcEStages;
+        p.ctas_per_sm = 1;
+        p.n_groups = (rows + 7) / 8;
+        return p;
+    }
     const bool use_rowwarp =
         m == 1 && (t.m1_kernel == 1 ||
                    (t.m1_kernel == 0 && rows * cols * bpw >= t.m1_rowwarp_min_bytes));
@@ -412,6 +499,14 @@ int fp8blk_set_launch_tuning(int target_stage_bytes, int ctas_per_sm, int use_pd
     return FP8BLK_OK;
 }
 
+int fp8blk_set_tensor_core_min_m(int min_m, int64_t min_bytes) {
+    if (min_m != 0 && (min_m < 2 || min_m > FP8BLK_MAX_M + 1)) return FP8BLK_EINVAL;
+    if (min_bytes < 0) return FP8BLK_EINVAL;
+    tuning().tc_min_m = min_m == 0 ? Tuning().tc_min_m : min_m;
+    tuning().tc_min_bytes = min_bytes == 0 ? Tuning().tc_min_bytes : min_bytes;
+    return FP8BLK_OK;
+}
+
 int fp8blk_set_m1_kernel(int choice, int64_t rowwarp_min_bytes) {
     if (choice < 0 || choice > 2 || rowwarp_min_bytes < 0) return FP8BLK_EINVAL;
     tuning().m1_kernel = choice;
@@ -434,10 +529,10 @@ int fp8blk_plan_query(int m, int64_t rows, int64_t cols, int bytes_per_weight, i
     const int team_warps = 1 << p.team_warps_log2;
     out[0] = p.panels;
     out[1] = p.panel_cols;
-    out[2] = p.kind == kRowWarpKernel ? 1 : team_warps;
-    out[3] = p.kind == kRowWarpKernel ? kRowWarps : kWarps / team_warps;
+    out[2] = p.kind == kTeamKernel ? team_warps : 1;
+    out[3] = p.kind == kRowWarpKernel ? kRowWarps : (p.kind == kTensorCoreKernel ? kTcConvWarps : kWarps / team_warps);
     out[4] = p.rb;
-    out[5] = p.kind == kRowWarpKernel ? 1 : 8 / pow2_ceil(m);
+    out[5] = p.kind == kTeamKernel ? 8 / pow2_ceil(m) : 1;
     out[6] = p.stage_rows;
     out[7] = p.stage_bytes;
     out[8] = p.stages;

@@ -59,13 +59,30 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 
+// try_wait without a suspend hint: returns after a short hardware-chosen
+// interval; for a thread on the critical path that must react at once.
+__device__ __forceinline__ bool mbar_try_wait_short(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
 // Waits for phase `parity` of the barrier to complete, for at most
-// kWaitLimitNs.  Returns false on expiry.
+// kWaitLimitNs.  Returns false on expiry.  SLEEP = false polls without the
+// suspend hint.
+template <bool SLEEP = true>
 __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity) {
-    if (mbar_try_wait(bar, parity)) return true;
+    auto poll = [&]() { return SLEEP ? mbar_try_wait(bar, parity) : mbar_try_wait_short(bar, parity); };
+    if (poll()) return true;
     const uint64_t t0 = global_timer_ns();
     while (true) {
-        if (mbar_try_wait(bar, parity)) return true;
+        if (poll()) return true;
         if (global_timer_ns() - t0 > kWaitLimitNs) return false;
     }
 }

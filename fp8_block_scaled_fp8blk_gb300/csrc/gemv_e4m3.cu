@@ -13,6 +13,7 @@ static cudaError_t launch_m(const GemvArgs &a, const Plan &p, bool argmax, const
 
 cudaError_t launch_gemv_e4m3(const GemvArgs &a, const Plan &p, int m, bool argmax,
                              const DeviceInfo &dev, cudaStream_t stream) {
+    if (p.kind == kTensorCoreKernel) return launch_gemv_tc(a, p, m, argmax, dev, stream);
     if (p.kind == kRowWarpKernel) {
         if (argmax) return launch_stream_kernel(rowwarp_gemv_kernel<kE4M3, true>, a, p, dev, stream);
         return launch_stream_kernel(rowwarp_gemv_kernel<kE4M3, false>, a, p, dev, stream);

@@ -8,6 +8,7 @@
 
 #include "rowwarp_gemv.cuh"
 #include "stream_gemv.cuh"
+#include "tc_gemv.cuh"
 
 namespace fp8blk {
 
@@ -20,6 +21,8 @@ struct Tuning {
     int l2_prefetch = 1;                 // L2 prefetch of the first stages before the PDL wait
     int max_stages = kMaxStages;
     int m1_kernel = 0;                   // m = 1: 0 = by size, 1 = row-per-warp, 2 = team
+    int tc_min_m = 5;                    // tensor-core kernel for m >= this (9 = never)
+    int64_t tc_min_bytes = 32ll << 20;   // ... and at least this many weight bytes
     int64_t m1_rowwarp_min_bytes = 96ll << 20;  // by size: row-per-warp from this many weight bytes
 };
 Tuning &tuning();
@@ -34,7 +37,7 @@ struct DeviceInfo {
 cudaError_t current_device_info(DeviceInfo *out);
 
 // Geometry of one streaming-GEMV launch (see GemvArgs).
-enum PlanKind : int { kTeamKernel = 0, kRowWarpKernel = 1 };
+enum PlanKind : int { kTeamKernel = 0, kRowWarpKernel = 1, kTensorCoreKernel = 2 };
 struct Plan {
     int kind = kTeamKernel;  // m = 1 uses the row-per-warp kernel
     int panels = 1;
@@ -56,7 +59,18 @@ Plan make_plan(int m, int64_t rows, int64_t cols, int bpw, const DeviceInfo &dev
 // Fill GemvArgs geometry from a plan.
 void apply_plan(const Plan &p, GemvArgs *a);
 
-// Kernel launches (defined in gemv_e4m3.cu / gemv_bf16.cu / nvfp4_dequant.cu).
+// Tensor map of an e4m3 weight matrix for the tensor-core kernel: 2-D,
+// {cols, rows}, boxes of box_rows rows x 128 bytes, 128-byte swizzle.  Cached
+// per (pointer, shape, box height).
+cudaError_t weight_tensor_map(const uint8_t *w, int64_t rows, int64_t cols, int box_rows, CUtensorMap *out);
+// Tensor map of the m x cols f32 activations: boxes of all m rows x box_cols
+// columns, no swizzle, zeros out of range.  Cached per (pointer, m, cols).
+cudaError_t activation_tensor_map(const float *x, int m, int64_t cols, int box_cols, CUtensorMap *out);
+
+// Kernel launches (defined in gemv_e4m3.cu / gemv_bf16.cu / nvfp4_dequant.cu /
+// gemv_tc.cu).
+cudaError_t launch_gemv_tc(const GemvArgs &a, const Plan &p, int m, bool argmax, const DeviceInfo &dev,
+                           cudaStream_t stream);
 cudaError_t launch_gemv_e4m3(const GemvArgs &a, const Plan &p, int m, bool argmax,
                              const DeviceInfo &dev, cudaStream_t stream);
 cudaError_t launch_gemv_bf16(const GemvArgs &a, const Plan &p, int m, const DeviceInfo &dev,
@@ -73,6 +87,7 @@ cudaError_t kernel_occupancy(const void *kernel, int threads, size_t smem, int *
 
 // Dynamic shared memory of a planned launch.
 inline size_t plan_smem_bytes(const Plan &p) {
+    if (p.kind == kTensorCoreKernel) return kTcSmemBytes;
     if (p.kind == kRowWarpKernel) return static_cast<size_t>(kRowWarps) * p.stages * p.stage_bytes;
     return static_cast<size_t>(p.stages) * p.stage_bytes;
 }

@@ -272,7 +272,7 @@ __device__ __forceinline__ void warp_argmax_merge(float &v, uint32_t &i) {
     }
 }
 
-constexpr int kAmWarps = 8;  // rows of the argmax merge scratch (one per warp)
+constexpr int kAmWarps = 16;  // rows of the argmax merge scratch (one per warp)
 
 // Called by every thread of the CTA after its per-activation-row partials
 // (part_val/part_idx[blockIdx.x * M + i]) are stored.  Publishes them; the last

@@ -54,6 +54,8 @@ _lib.fp8blk_set_launch_tuning.restype = _INT
 _lib.fp8blk_set_launch_tuning.argtypes = [_INT, _INT, _INT, _INT, _INT]
 _lib.fp8blk_set_m1_kernel.restype = _INT
 _lib.fp8blk_set_m1_kernel.argtypes = [_INT, _I64]
+_lib.fp8blk_set_tensor_core_min_m.restype = _INT
+_lib.fp8blk_set_tensor_core_min_m.argtypes = [_INT, _I64]
 _lib.fp8blk_plan_query.restype = _INT
 _lib.fp8blk_plan_query.argtypes = [_INT, _I64, _I64, _INT, _INT, _INT, _INT, _P]
 _lib.fp8blk_device_status.restype = _INT
@@ -248,6 +250,12 @@ def plan_query(m: int, rows: int, cols: int, bytes_per_weight: int = 1, sms: int
 def set_m1_kernel(choice: int = 0, rowwarp_min_bytes: int = 0) -> None:
     """m = 1 kernel: 0 by size, 1 row-per-warp, 2 team (speed only)."""
     _check(_lib.fp8blk_set_m1_kernel(choice, rowwarp_min_bytes), "fp8blk_set_m1_kernel")
+
+
+def set_tensor_core_min_m(min_m: int = 0, min_bytes: int = 0) -> None:
+    """e4m3 GEMVs with m >= min_m (2..8; 9 = never) and at least min_bytes of
+    weights (1 = any) run on the tensor cores; 0 restores a default."""
+    _check(_lib.fp8blk_set_tensor_core_min_m(min_m, min_bytes), "fp8blk_set_tensor_core_min_m")
 
 
 def fp8blk_device_status(clear: bool = False) -> int:

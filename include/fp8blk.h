@@ -225,6 +225,24 @@ int fp8blk_set_launch_tuning(int target_stage_bytes, int ctas_per_sm, int use_pd
 int fp8blk_set_m1_kernel(int choice, int64_t rowwarp_min_bytes);
 
 /*
+ * fp8blk_set_tensor_core_min_m -- route e4m3 GEMVs with m >= min_m activation
+ * rows (2..8; 9 = never; 0 = the library default, 5) and at least min_bytes
+ * of weights (rows * cols; 1 = any size; 0 = the library default, 32 MiB) to
+ * the tensor-core kernel ("Struct Dsv4Gpu" page,
+ * verify_batch_dev: the k+1 rows of a speculative verify).  That kernel
+ * re-encodes each 128 x 128 weight tile as f16 (e4m3 value times the block
+ * scale, exact after a per-128-row power-of-two offset), splits x into two
+ * f16 planes (about 22 significant bits) and accumulates on the tensor cores
+ * in f32.  The result stays within the e4m3 GEMV error bound but is not
+ * bit-identical to the CUDA-core kernels.  Row blocks whose scales are not
+ * positive finite powers of two, or span more than 2^22, are computed by a
+ * CUDA-core loop in the same launch.  Speed only; process-wide; not
+ * thread-safe against concurrent calls of the other entry points.
+ * Errors: EINVAL.
+ */
+int fp8blk_set_tensor_core_min_m(int min_m, int64_t min_bytes);
+
+/*
  * fp8blk_plan_query -- HOST, no CUDA calls: the launch geometry the streaming
  * GEMV would use for this shape on a device with the given SM count and
  * shared-memory limits (bytes), for inspection and bounds checks.

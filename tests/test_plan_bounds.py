@@ -10,6 +10,8 @@ import pytest
 GB300 = dict(sms=152, smem_per_sm=233472, smem_per_block=232448)
 STATIC_SMEM = 4736 + 128  # team kernel: red/argmax buffers, barriers, counters (ptxas report)
 ROWWARP_STATIC_SMEM = 1024  # row-per-warp kernel: barriers + argmax scratch
+TC_STATIC_SMEM = 2048  # tensor-core kernel: barriers, tables, argmax scratch (ptxas report)
+TC_MAX_ROW_BLOCKS, TC_MAX_SF = 64, 4096
 MAX_GRID = 1024
 
 
@@ -50,8 +52,33 @@ def _check_partition(n_groups, workers):
     assert all(ends[i][1] == ends[i + 1][0] for i in range(workers - 1))
 
 
+def check_tc_plan(p, m, rows, cols, bpw):
+    """Tensor-core kernel: one CTA per SM over whole 8-row units; panels of
+    4096 columns (TMA boxes start on 128-column boundaries); the CTA's scale
+    row blocks and their f16 factors must fit the shared tables."""
+    assert m >= 2 and bpw == 1 and cols >= 128
+    pc, panels = p["panel_cols"], p["panels"]
+    assert pc == (cols if panels == 1 else 4096)
+    assert (panels - 1) * pc < cols <= panels * pc
+    n_units8 = -(-rows // 8)
+    assert p["n_groups"] == n_units8 and p["ctas_per_sm"] == 1
+    grid = min(GB300["sms"], n_units8, MAX_GRID)
+    _check_partition(n_units8, grid)
+    gcols = -(-cols // 128)
+    for b in range(grid):
+        u0, u1 = b * n_units8 // grid, (b + 1) * n_units8 // grid
+        r0, r1 = u0 * 8, min(u1 * 8, rows)
+        assert r1 > r0
+        n_rb = ((r1 - 1) >> 7) - (r0 >> 7) + 1
+        assert n_rb <= TC_MAX_ROW_BLOCKS and n_rb * gcols <= TC_MAX_SF
+    assert p["dynamic_smem_bytes"] + TC_STATIC_SMEM <= GB300["smem_per_block"]
+    return p
+
+
 def check_plan(ops, m, rows, cols, bpw):
     p = ops.plan_query(m, rows, cols, bpw, **GB300)
+    if p["kernel"] == 2:
+        return check_tc_plan(p, m, rows, cols, bpw)
     _check_common(p, rows, cols, bpw)
     pc, tw, teams = p["panel_cols"], p["team_warps"], p["teams"]
     R, sb, ns, dyn = p["stage_rows"], p["stage_bytes"], p["stages"], p["dynamic_smem_bytes"]
@@ -98,10 +125,24 @@ def test_plans_stay_in_bounds(ops, bpw, m1_kernel):
         ops.set_m1_kernel(0)
 
 
+def test_tensor_core_plans_stay_in_bounds(ops):
+    ops.set_tensor_core_min_m(2, 1)  # every m >= 2 shape that qualifies
+    try:
+        seen = 0
+        for m, rows, cols in SHAPES + [(8, 1_000_000, 4096), (5, 300_000, 16384), (2, 8, 128)]:
+            p = check_plan(ops, m, rows, cols, 1)
+            seen += p["kernel"] == 2
+        assert seen > 100
+    finally:
+        ops.set_tensor_core_min_m(0, 0)
+
+
 def test_headline_plans(ops):
     p = check_plan(ops, 1, 4096, 4096, 1)
     assert p["panels"] == 1 and p["kernel"] == 0  # small: team kernel
     p = check_plan(ops, 1, 131072, 4096, 1)
     assert p["kernel"] == 1  # large: row-per-warp
     p = check_plan(ops, 8, 16384, 4096, 1)
-    assert p["ctas_per_sm"] == 1
+    assert p["kernel"] == 2 and p["ctas_per_sm"] == 1  # batched verify: tensor cores
+    assert check_plan(ops, 4, 16384, 4096, 1)["kernel"] == 0  # m = 4: CUDA cores
+    assert check_plan(ops, 8, 2048, 4096, 1)["kernel"] == 0  # small: CUDA cores

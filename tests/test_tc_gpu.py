@@ -1,0 +1,191 @@
+"""GPU parity of the tensor-core e4m3 GEMV (m >= 2, forced on) against the
+CPU oracle, through the C ABI.
+
+The kernel re-encodes each weight tile as exact f16 (e4m3 value times the
+block scale times a per-128-row power of two), splits x into two f16 planes
+and accumulates on the tensor cores in f32.  Bar: the same per-element bound as
+the CUDA-core kernels, |gpu - oracle| <= 1e-5 * sum_c |w x| + 1e-6; bit-exact
+invariants where the encoding makes them exact (one-hot x, negation,
+power-of-two scaling of x or of the whole scale grid, run-to-run); the
+CUDA-core fallback for scale grids the f16 encoding cannot carry; the fused
+argmax.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from _helpers import ABS, REL, assert_close, scales_dev, to_dev
+from fp8_block_scaled_fp8blk_gb300 import synth
+
+pytestmark = pytest.mark.gpu
+
+TC_KIND = 2
+
+
+@pytest.fixture(scope="module")
+def ops():
+    from fp8_block_scaled_fp8blk_gb300 import ops as o
+    o.set_tensor_core_min_m(2, 1)
+    yield o
+    o.set_tensor_core_min_m(0, 0)
+    assert o.fp8blk_device_status(clear=True) == 0
+
+
+def run(ops, codes, scales_f32, x):
+    y = ops.fp8blk_gemv(to_dev(codes), to_dev(scales_f32), to_dev(x))
+    torch.cuda.synchronize()
+    return y.cpu().numpy()
+
+
+def run_case(ops, case):
+    return run(ops, case.codes, ops.fp8blk_scales_from_e8m0(case.scale_e8m0), case.x)
+
+
+# m >= 2; ragged rows (not multiples of 8 or 128, fewer rows than 8), ragged
+# K-blocks (cols not a multiple of 128), several column panels, and shapes
+# with cols < 128 that the planner keeps on the CUDA-core kernel.
+SHAPES = [(2, 257, 400), (3, 1000, 1040), (4, 129, 4096), (5, 77, 4112), (6, 300, 144),
+          (7, 515, 2064), (8, 257, 8208), (8, 640, 4096), (2, 96, 12304), (2, 7, 128),
+          (8, 1, 128), (3, 5000, 256), (4, 2, 48), (8, 300, 16),
+          # CTAs with several 128-row tiles (full-height and short boxes) that
+          # straddle scale row blocks, one and several panels
+          (3, 40000, 1040), (8, 20000, 8208), (2, 16384, 4096)]
+
+
+def test_tc_plan_selected(ops):
+    out = ops.plan_query(8, 16384, 4096, bytes_per_weight=1)
+    assert out["kernel"] == TC_KIND
+    assert ops.plan_query(8, 300, 16, bytes_per_weight=1)["kernel"] != TC_KIND
+    assert ops.plan_query(1, 16384, 4096, bytes_per_weight=1)["kernel"] != TC_KIND
+
+
+@pytest.mark.parametrize("m,rows,cols", SHAPES)
+def test_tc_matches_oracle_ragged(ops, m, rows, cols):
+    case = synth.fp8blk_case(rows, cols, m, seed=5000 + rows + cols + m)
+    y = run_case(ops, case)
+    ref, a = oracle.fp8blk_gemv(case.codes, case.scale_e8m0, case.x, nthreads=8)
+    assert_close(y, ref, a, f"tc m={m} {rows}x{cols}")
+
+
+def test_tc_verify_16384x4096_m8_full(ops):
+    case = synth.workload_case("verify_16384x4096_m8")
+    y = run_case(ops, case)
+    ref, a = oracle.fp8blk_gemv(case.codes, case.scale_e8m0, case.x, nthreads=16)
+    assert_close(y, ref, a, "tc verify_16384x4096_m8")
+
+
+def test_tc_x_wide_dynamic_range(ops):
+    """x spanning 2^-60 .. 2^60 within one row: the f16 planes are scaled per
+    activation row, so small elements lose at most 2^-40 of the row maximum."""
+    rows, cols, m = 640, 4096, 4
+    case = synth.fp8blk_case(rows, cols, m, seed=77)
+    rng = np.random.default_rng(78)
+    case.x *= np.exp2(rng.integers(-60, 61, size=case.x.shape)).astype(np.float32)
+    y = run_case(ops, case)
+    ref, a = oracle.fp8blk_gemv(case.codes, case.scale_e8m0, case.x, nthreads=8)
+    assert_close(y, ref, a, "tc wide x range")
+
+
+def test_tc_scale_spread_at_limit_and_beyond(ops):
+    """Within a 128-row block a scale spread of 2^22 still runs on the tensor
+    cores (weights down to 2^-24 stay exact f16); 2^23 and beyond take the
+    CUDA-core fallback.  Both must match the oracle, with blocks of either kind
+    in one launch."""
+    rows, cols, m = 2048, 1024, 3
+    case = synth.fp8blk_case(rows, cols, m, seed=79)
+    g = case.scale_e8m0
+    g[0, :] = 111
+    g[0, 0], g[0, 1] = 100, 122          # spread 22: tensor cores
+    g[5, 2], g[5, 3] = 10, 200           # spread 190: fallback
+    g[9, :] = 127
+    g[9, 7] = 150                        # spread 23: fallback
+    g[15, 0], g[15, 7] = 30, 220         # 2^-97 .. 2^93 (sums stay finite in f32): fallback
+    y = run_case(ops, case)
+    ref, a = oracle.fp8blk_gemv(case.codes, case.scale_e8m0, case.x, nthreads=8)
+    assert_close(y, ref, a, "tc scale spread")
+
+
+def test_tc_non_power_of_two_scales_take_fallback(ops):
+    """Scales passed as arbitrary f32 (not e8m0): the f16 encoding is not
+    exact, so those blocks take the CUDA-core loop; checked against the plain
+    definition sum_c w[r][c] * S[r/128][c/128] * x[i][c] in double."""
+    rows, cols, m = 384, 512, 2
+    case = synth.fp8blk_case(rows, cols, m, seed=80)
+    sf = ops.fp8blk_scales_from_e8m0(case.scale_e8m0).copy()
+    sf[1, 2] *= 1.5
+    y = run(ops, case.codes, sf, case.x)
+    wv = oracle.e4m3_table()[case.codes] * np.repeat(np.repeat(sf.astype(np.float64), 128, 0), 128, 1)[:rows, :cols]
+    ref = case.x.astype(np.float64) @ wv.T
+    a = np.abs(case.x.astype(np.float64)) @ np.abs(wv).T
+    assert_close(y, ref, a, "tc non-pow2 scales")
+
+
+def test_tc_one_hot_exact_and_invariants(ops):
+    rows, cols, m = 520, 1040, 4
+    rng = np.random.default_rng(81)
+    codes = synth.finite_e4m3_codes(rng, (rows, cols))
+    scale = synth.e8m0_codes(rng, ((rows + 127) // 128, (cols + 127) // 128), -10, 10)
+    sf = ops.fp8blk_scales_from_e8m0(scale)
+    # one-hot rows of x reproduce decoded weight columns exactly
+    cs = [0, 129, 1039, 640]
+    x = np.zeros((m, cols), dtype=np.float32)
+    for i, c in enumerate(cs):
+        x[i, c] = 1.0
+    y = run(ops, codes, sf, x)
+    dec = oracle.e4m3_table()[codes]
+    for i, c in enumerate(cs):
+        want = (dec[:, c] * sf[np.arange(rows) // 128, c // 128]).astype(np.float32)
+        assert np.array_equal(y[i], want)
+    xr = rng.standard_normal((m, cols), dtype=np.float32)
+    y0 = run(ops, codes, sf, xr)
+    assert np.array_equal(run(ops, codes, sf, xr), y0), "run to run"
+    assert np.array_equal(run(ops, codes, sf, -xr), -y0), "negation"
+    assert np.array_equal(run(ops, codes, sf, xr * np.float32(2.0 ** -9)), y0 * np.float32(2.0 ** -9))
+    assert np.array_equal(run(ops, codes, sf * np.float32(2.0 ** 5), xr), y0 * np.float32(2.0 ** 5))
+
+
+def test_tc_nan_code_only_poisons_its_row(ops):
+    case = synth.fp8blk_case(300, 512, 3, seed=82)
+    case.codes[133, 300] = 0x7F
+    y = run_case(ops, case)
+    assert np.isnan(y[:, 133]).all()
+    assert not np.isnan(np.delete(y, 133, axis=1)).any()
+
+
+@pytest.mark.parametrize("m,rows,cols", [(2, 4097, 1040), (3, 1000, 272), (8, 640, 4096),
+                                         (2, 300, 8208), (5, 129, 4112), (8, 16384, 4096)])
+def test_tc_argmax_matches_oracle(ops, m, rows, cols):
+    case = synth.fp8blk_case(rows, cols, m, seed=rows + cols + 11 * m)
+    w, s, x = to_dev(case.codes), scales_dev(case.scale_e8m0), to_dev(case.x)
+    ws = ops.argmax_workspace(m, rows, cols, "cuda:0")
+    logits = torch.empty((m, rows), dtype=torch.float32, device="cuda:0")
+    tok = ops.fp8blk_gemv_argmax(w, s, x, ws, logits=logits).cpu().numpy().view(np.uint32)
+    lg = logits.cpu().numpy()
+    ref, a = oracle.fp8blk_gemv(case.codes, case.scale_e8m0, case.x, nthreads=16)
+    assert_close(lg, ref, a, f"tc argmax logits m={m} {rows}x{cols}")
+    for i in range(m):
+        assert tok[i] == oracle.argmax(lg[i].astype(np.float64))
+        srt = np.sort(ref[i])[::-1]
+        if srt.size > 1 and srt[0] - srt[1] > 2 * (REL * a[i].max() + ABS):
+            assert tok[i] == oracle.argmax(ref[i])
+    tok2 = ops.fp8blk_gemv_argmax(w, s, x, ws).cpu().numpy().view(np.uint32)
+    assert np.array_equal(tok, tok2)
+
+
+def test_tc_argmax_ties_resolve_to_lowest_index(ops):
+    rows, cols, m = 2048, 1024, 2
+    case = synth.fp8blk_case(rows, cols, m, seed=83)
+    case.scale_e8m0[...] = 127
+    case.x[...] = np.abs(case.x) + 0.01
+    case.codes &= np.uint8(0x37)
+    for r in (9, 10, 700, 2047):
+        case.codes[r] = 0x38
+    w, s, x = to_dev(case.codes), scales_dev(case.scale_e8m0), to_dev(case.x)
+    ws = ops.argmax_workspace(m, rows, cols, "cuda:0")
+    tok = ops.fp8blk_gemv_argmax(w, s, x, ws).cpu().numpy().view(np.uint32)
+    assert list(tok) == [9, 9]
+
+
+def test_tc_device_status_clean(ops):
+    assert ops.fp8blk_device_status() == 0
