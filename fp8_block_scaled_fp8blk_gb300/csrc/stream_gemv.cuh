@@ -278,11 +278,11 @@ constexpr int kAmWarps = 16;  // rows of the argmax merge scratch (one per warp)
 // (part_val/part_idx[blockIdx.x * M + i]) are stored.  Publishes them; the last
 // CTA to arrive merges all CTAs' partials in CTA order and writes the tokens.
 // The arrival counter wraps back to 0, ready for the next call.
-template <int M, int NT>
-__device__ __forceinline__ void argmax_cross_cta(const GemvArgs &a, float (&am_val)[kAmWarps][8],
-                                                 uint32_t (&am_idx)[kAmWarps][8], int *s_is_last) {
+template <int M, int NT, int AW>
+__device__ __forceinline__ void argmax_cross_cta(const GemvArgs &a, float (&am_val)[AW][8], uint32_t (&am_idx)[AW][8],
+                                                 int *s_is_last) {
     constexpr int NW = NT / 32;
-    static_assert(NW <= kAmWarps, "argmax scratch too small");
+    static_assert(NW <= AW, "argmax scratch too small");
     __threadfence();
     __syncthreads();
     if (threadIdx.x == 0) *s_is_last = (atomicInc(a.counter, gridDim.x - 1) == gridDim.x - 1);

@@ -25,13 +25,19 @@
 //                  are few and large.  The weight boxes of the first stages are
 //                  issued before the grid dependency wait (weights are never
 //                  outputs of the preceding kernel), x only after it;
-//   converter warps: e4m3 tile -> f16 A tile in the UMMA K-major layout (no
-//                  swizzle: 8 x 16-byte core matrices, LBO = 128 B along K,
-//                  SBO = 2048 B per 8 rows) and, all of them together, the x
-//                  slice -> B tile; the first four warps also run the epilogue;
-//   MMA warp, lane 0: 8 x tcgen05.mma (K = 16 each) per K-block, commits to
-//                  mbarriers that free the operand stage / publish the
-//                  accumulator (two accumulators of 16 columns alternate).
+//   converter warps: each thread converts one tile row's K slice (two warps
+//                  per 32-lane quarter of tensor memory) to f16 and stores it
+//                  into its own TMEM lane (tcgen05.st; row r in lane r, two f16
+//                  of consecutive K per 32-bit column), and all of them build
+//                  the 16 x 128 B tile in shared memory from the x slice (UMMA
+//                  K-major, no swizzle: 8 x 16-byte core matrices, LBO = 128 B,
+//                  SBO = 2048 B); the first four warps also run the epilogue;
+//   MMA warp, lane 0: 8 x tcgen05.mma (K = 16 each, A from tensor memory, B
+//                  from shared memory) per K-block, commits to mbarriers that
+//                  free the operand stage / publish the accumulator (two
+//                  accumulators of 16 columns alternate).
+// Keeping A in tensor memory spares shared memory the f16 tile's write and the
+// tensor core's read of it (64 KiB per K-block), which bounded the rate.
 // The f16 scale factors S * 2^-q are tabulated in shared memory before the
 // roles split.
 // Every wait is a bounded mbarrier wait; any timeout raises a shared abort
@@ -50,16 +56,19 @@
 #define TC_CONV_WARPS 8
 #endif
 #ifndef TC_E_STAGES
-#define TC_E_STAGES 3
-#endif
-#ifndef TC_AK
-#define TC_AK 128
+#define TC_E_STAGES 4
 #endif
 #ifndef TC_AB_STAGES
-#define TC_AB_STAGES (2 * 128 / TC_AK)
+#define TC_AB_STAGES 4
 #endif
 #ifndef TC_SPIN
 #define TC_SPIN 0
+#endif
+#ifndef TC_MMA_WARPS
+#define TC_MMA_WARPS 2
+#endif
+#ifndef TC_B_WARPS
+#define TC_B_WARPS 4
 #endif
 #ifndef TC_MMA_SLEEP
 #define TC_MMA_SLEEP 0
@@ -73,14 +82,18 @@ constexpr int kTcKb = 128;         // columns per K-block (one scale block, one 
 constexpr int kTcKbPerStage = 2;   // K-blocks per TMA ring stage
 constexpr int kTcConvWarps = TC_CONV_WARPS;  // converters; the first 4 also run the epilogue
 constexpr int kTcEpiWarps = 4;
-constexpr int kTcProducerWarp = kTcConvWarps;
-constexpr int kTcMmaWarp = kTcConvWarps + 1;
-constexpr int kTcThreads = (kTcConvWarps + 2) * 32;
-constexpr int kTcGroupsPerWarp = (kTcM / 8) / kTcConvWarps;  // 8-row groups each converter owns
+constexpr int kTcBWarp0 = kTcConvWarps;                // warps that build the B tile
+constexpr int kTcBWarps = TC_B_WARPS;
+constexpr int kTcProducerWarp = kTcBWarp0 + kTcBWarps;
+constexpr int kTcMmaWarp = kTcProducerWarp + 1;        // first MMA-issuing warp
+constexpr int kTcMmaWarps = TC_MMA_WARPS;              // MMA-issuing warps (one lane each)
+constexpr int kTcStageArrivals = kTcConvWarps + kTcBWarps;  // warps that fill / release a stage
+constexpr int kTcThreads = (kTcProducerWarp + 1 + kTcMmaWarps) * 32;
+constexpr int kTcKSplit = kTcConvWarps / 4;        // converter warps per TMEM lane quarter
+constexpr int kTcKW = kTcKb / kTcKSplit;            // K columns each converter thread converts
+constexpr int kTcChunks = kTcKW / 16;               // ... as 16-code chunks
 constexpr int kTcEStages = TC_E_STAGES;   // TMA ring depth
-constexpr int kTcAK = TC_AK;              // columns per operand stage (a K-block or half of one)
-constexpr int kTcSub = 128 / kTcAK;       // operand stages per K-block
-constexpr int kTcStages = TC_AB_STAGES;   // f16 A + B ring depth (MMA operands)
+constexpr int kTcStages = TC_AB_STAGES;   // operand ring depth: A in tensor memory, B in shared memory
 constexpr bool kTcSleep = TC_SPIN == 0;   // converters' and producer's waits: sleeping (true) or polling
 constexpr bool kTcMmaSleep = TC_MMA_SLEEP != 0;  // MMA issuer's waits
 constexpr int kTcMaxPanel = 4096;         // columns per panel
@@ -88,22 +101,28 @@ constexpr int kTcETileBytes = kTcM * kTcKb;          // 16 KiB of e4m3 codes per
 constexpr int kTcXCols = kTcKbPerStage * kTcKb;      // x columns per stage (one 2-D box)
 constexpr int kTcXStageBytes = 8 * kTcXCols * 4;     // up to 8 rows x 256 f32
 constexpr int kTcEStageBytes = kTcKbPerStage * kTcETileBytes + kTcXStageBytes;
-constexpr int kTcATileBytes = kTcM * kTcAK * 2;      // 16 or 32 KiB
-constexpr int kTcBTileBytes = kTcN * kTcAK * 2;      // 2 or 4 KiB
-constexpr int kTcSbo = kTcAK / 8 * 128;              // bytes between 8-row core groups (A and B)
-constexpr int kTcABStageBytes = kTcATileBytes + kTcBTileBytes;
+constexpr int kTcBTileBytes = kTcN * kTcKb * 2;      // 4 KiB
+constexpr int kTcSbo = kTcKb / 8 * 128;              // bytes between the B tile's 8-row core groups
 constexpr int kTcMaxSf = 4096;                       // f16 scale factors held in shared memory
-constexpr int kTcTmemCols = 2 * kTcN;
+constexpr int kTcACols = kTcKb / 2;                  // TMEM columns of one A stage (two f16 per column)
+constexpr int kTcDCol = kTcStages * kTcACols;        // first accumulator column
+// A tcgen05.mma costs its issuing thread about 120 cycles whatever the
+// shape, so the 8 MMAs of a K-block are spread over kTcMmaWarps warps, each
+// into its own accumulator (K-steps interleaved); the epilogue adds them.
+constexpr int kTcNAcc = kTcMmaWarps;
+constexpr int kTcDBuf = kTcNAcc * kTcN;              // accumulator columns per tile buffer
+constexpr int kTcTmemUsed = kTcDCol + 2 * kTcDBuf;
+constexpr int kTcTmemCols = kTcTmemUsed <= 64 ? 64 : kTcTmemUsed <= 128 ? 128 : kTcTmemUsed <= 256 ? 256 : 512;
 constexpr int kTcSmemBytes =
-    kTcEStages * kTcEStageBytes + kTcStages * kTcABStageBytes + kTcMaxSf * 2 + 1024;  // + alignment slack
+    kTcEStages * kTcEStageBytes + kTcStages * kTcBTileBytes + kTcMaxSf * 2 + 1024;  // + alignment slack
 constexpr int kTcMaxRowBlocks = 64;                  // scale row blocks a CTA may span
 constexpr int kTcSmallBoxRows = 32;                  // tiles this short load one 32-row box per K-block
 static_assert(kTcEStageBytes % 1024 == 0, "swizzled TMA tiles need 1024-byte alignment");
-static_assert((kTcM / 8) % kTcConvWarps == 0, "row groups must split evenly");
-static_assert(kTcConvWarps == 4 || kTcConvWarps == 8, "4 or 8 converter warps");
-constexpr int kTcBValsPerThread = 8 * kTcAK / (kTcConvWarps * 32);  // x values each converter thread encodes
-static_assert(kTcBValsPerThread == 2 || kTcBValsPerThread == 4 || kTcBValsPerThread == 8, "B split");
-static_assert(kTcAK == 64 || kTcAK == 128, "operand stage width");
+static_assert(kTcConvWarps == 8 || kTcConvWarps == 16, "8 or 16 converter warps");
+static_assert(kTcTmemUsed <= 512, "tensor memory holds 512 columns");
+static_assert((kTcKb / 16) % kTcMmaWarps == 0, "K-steps split evenly over the MMA warps");
+constexpr int kTcBValsPerThread = 8 * kTcKb / (kTcBWarps * 32);  // x values each B thread encodes
+static_assert(kTcBValsPerThread == 16 || kTcBValsPerThread == 8, "B split: 8 or 16 values (whole K-cores)");
 
 struct TcArgs {
     const float *scales;
@@ -180,6 +199,42 @@ __device__ __forceinline__ void tc_ld16(uint32_t taddr, float (&v)[16]) {
     for (int j = 0; j < 16; ++j) v[j] = __uint_as_float(r[j]);
 }
 
+// One warp stores N consecutive 32-bit columns of its own 32 TMEM lanes.
+template <int N>
+__device__ __forceinline__ void tc_st(uint32_t taddr, const uint32_t (&v)[N]);
+
+template <>
+__device__ __forceinline__ void tc_st<16>(uint32_t taddr, const uint32_t (&v)[16]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr),
+        "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]), "r"(v[9]),
+        "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
+        : "memory");
+}
+
+template <>
+__device__ __forceinline__ void tc_st<32>(uint32_t taddr, const uint32_t (&v)[32]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+        "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+        "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]), "r"(v[9]),
+        "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15]), "r"(v[16]), "r"(v[17]), "r"(v[18]),
+        "r"(v[19]), "r"(v[20]), "r"(v[21]), "r"(v[22]), "r"(v[23]), "r"(v[24]), "r"(v[25]), "r"(v[26]), "r"(v[27]),
+        "r"(v[28]), "r"(v[29]), "r"(v[30]), "r"(v[31])
+        : "memory");
+}
+
+// kind::f16 MMA with A read from tensor memory (row r in lane r, two f16 of
+// consecutive K per 32-bit column) and B from shared memory.
+__device__ __forceinline__ void tc_mma_f16_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                              bool accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(static_cast<uint32_t>(accumulate))
+        : "memory");
+}
+
 // 2^e as an f32 for -126 <= e <= 127.
 __device__ __forceinline__ float pow2f_normal(int e) { return __int_as_float((e + 127) << 23); }
 
@@ -247,8 +302,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     __shared__ int s_q[kTcMaxRowBlocks];
     __shared__ int s_p[8];
     __shared__ int s_xmax_bits[8];
-    __shared__ float am_val[kAmWarps][8];
-    __shared__ uint32_t am_idx[kAmWarps][8];
+    __shared__ float s_xpart[kTcThreads];
+    __shared__ float am_val[kTcThreads / 32][8];
+    __shared__ uint32_t am_idx[kTcThreads / 32][8];
     __shared__ int s_is_last;
 
     const int tid = threadIdx.x;
@@ -261,8 +317,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     // ring: (f16 A tile 32 KiB | B tile 4 KiB) | f16 scale factors S * 2^-q
     // per (row block, K-block)].
     uint8_t *sE = tc_smem + ((1024u - (smem_addr(tc_smem) & 1023u)) & 1023u);
-    uint8_t *sAB = sE + kTcEStages * kTcEStageBytes;
-    __half *s_sf = reinterpret_cast<__half *>(sAB + kTcStages * kTcABStageBytes);
+    uint8_t *sB = sE + kTcEStages * kTcEStageBytes;
+    __half *s_sf = reinterpret_cast<__half *>(sB + kTcStages * kTcBTileBytes);
 
     // This CTA's rows: whole 8-row units, balanced.
     const int64_t u0 = static_cast<int64_t>(blockIdx.x) * a.n_units8 / gridDim.x;
@@ -284,14 +340,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     if (tid == 0) {
         for (int s = 0; s < kTcEStages; ++s) {
             mbar_init(smem_addr(&full_e[s]), 1);
-            mbar_init(smem_addr(&empty_e[s]), kTcConvWarps);
+            mbar_init(smem_addr(&empty_e[s]), kTcStageArrivals);
         }
         for (int s = 0; s < kTcStages; ++s) {
-            mbar_init(smem_addr(&conv_a[s]), kTcConvWarps);
-            mbar_init(smem_addr(&free_a[s]), 1);
+            mbar_init(smem_addr(&conv_a[s]), kTcStageArrivals);
+            mbar_init(smem_addr(&free_a[s]), kTcMmaWarps);
         }
         for (int s = 0; s < 2; ++s) {
-            mbar_init(smem_addr(&d_full[s]), 1);
+            mbar_init(smem_addr(&d_full[s]), kTcMmaWarps);
             mbar_init(smem_addr(&d_free[s]), kTcEpiWarps);
         }
         mbar_init_fence();
@@ -398,29 +454,40 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             for (int64_t kb = lane; kb < gcols; kb += 32)
                 s_sf[j * gcols + kb] = __float2half_rn(ldexpf(__ldg(srow + kb), 7 - emax));
         }
-        // max|x_i|: warp w takes row w (w < m), lanes stride its float4s with
-        // 8 independent loads in flight.
-        if (warp < m) {
+        // max|x_i|: threads [i * T, (i + 1) * T) take row i (T = threads per row),
+        // each every T-th float4 from its offset, up to 20 loads in flight; the
+        // partial maxima meet in s_xpart and one warp per row reduces them.
+        {
+            const int per_row = kTcThreads / m;
+            const int xi = tid / per_row;
+            const int j0 = tid - xi * per_row;
             const int c4n = static_cast<int>(a.cols / 4);
-            const float4 *xrow = reinterpret_cast<const float4 *>(a.x + static_cast<int64_t>(warp) * a.cols);
             float mxr = 0.f;
-            for (int j0 = lane; j0 < c4n; j0 += 8 * 32) {
-                float4 v[8];
+            if (xi < m) {
+                const float4 *xrow = reinterpret_cast<const float4 *>(a.x + static_cast<int64_t>(xi) * a.cols);
+                for (int jb = j0; jb < c4n; jb += 20 * per_row) {
+                    float4 v[20];
 #pragma unroll
-                for (int k = 0; k < 8; ++k) {
-                    const int j = j0 + k * 32;
-                    v[k] = j < c4n ? __ldg(xrow + j) : make_float4(0.f, 0.f, 0.f, 0.f);
+                    for (int k = 0; k < 20; ++k) {
+                        const int j = jb + k * per_row;
+                        v[k] = j < c4n ? __ldg(xrow + j) : make_float4(0.f, 0.f, 0.f, 0.f);
+                    }
+#pragma unroll
+                    for (int k = 0; k < 20; ++k)
+                        mxr = fmaxf(mxr, fmaxf(fmaxf(fabsf(v[k].x), fabsf(v[k].y)), fmaxf(fabsf(v[k].z), fabsf(v[k].w))));
                 }
-#pragma unroll
-                for (int k = 0; k < 8; ++k)
-                    mxr = fmaxf(mxr, fmaxf(fmaxf(fabsf(v[k].x), fabsf(v[k].y)), fmaxf(fabsf(v[k].z), fabsf(v[k].w))));
             }
-#pragma unroll
-            for (int off = 16; off >= 1; off >>= 1) mxr = fmaxf(mxr, __shfl_xor_sync(0xFFFFFFFFu, mxr, off));
-            const float v = mxr;
-            const int r = warp;
-            if (lane == 0 && v > 0.f) atomicMax(&s_xmax_bits[r], __float_as_int(v));
+            s_xpart[tid] = mxr;
         }
+    }
+    __syncthreads();
+    if (!s_fallback && warp < m) {
+        const int per_row = kTcThreads / m;
+        float v = 0.f;
+        for (int j = lane; j < per_row; j += 32) v = fmaxf(v, s_xpart[warp * per_row + j]);
+#pragma unroll
+        for (int off = 16; off >= 1; off >>= 1) v = fmaxf(v, __shfl_xor_sync(0xFFFFFFFFu, v, off));
+        if (lane == 0) s_xmax_bits[warp] = __float_as_int(v);  // non-negative: bits order like values
     }
     __syncthreads();
     if (tid < 8) {
@@ -481,8 +548,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             for (int64_t v = first_open; v < issued; ++v)
                 (void)mbar_wait_bounded(smem_addr(&full_e[v % kTcEStages]), static_cast<uint32_t>((v / kTcEStages) & 1));
         }
-    } else if (warp == kTcMmaWarp) {
-        // ---------------- MMA issuer
+    } else if (warp >= kTcMmaWarp) {
+        // ---------------- MMA issuers: warp kTcMmaWarp + j issues K-steps j, j + kTcMmaWarps, ...
+        // of every K-block into accumulator j.
+        const int mj = warp - kTcMmaWarp;
         if (lane == 0) {
             int64_t u = 0;
             int tile_seq = 0;
@@ -499,8 +568,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     }
                     tc_fence_after();
                     bool broke = false;
-                    const int nsub = nkb * kTcSub;
-                    for (int sb = 0; sb < nsub; ++sb, ++u) {
+                    for (int kb = 0; kb < nkb; ++kb, ++u) {
                         const int s = static_cast<int>(u % kTcStages);
                         if (!mbar_wait_bounded<kTcMmaSleep>(smem_addr(&conv_a[s]), static_cast<uint32_t>((u / kTcStages) & 1))) {
                             tc_raise_abort(&s_abort);
@@ -508,16 +576,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                             break;
                         }
                         tc_fence_after();
-                        const uint32_t a_base = smem_addr(sAB + s * kTcABStageBytes);
-                        const uint32_t b_base = a_base + kTcATileBytes;
+                        const uint32_t a_col = tmem + static_cast<uint32_t>(s * kTcACols);
+                        const uint32_t b_base = smem_addr(sB + s * kTcBTileBytes);
 #pragma unroll
-                        for (int k = 0; k < kTcAK / 16; ++k) {
-                            const uint64_t ad = umma_smem_desc(a_base + k * 256u, 128u, kTcSbo);
+                        for (int k = mj; k < kTcKb / 16; k += kTcMmaWarps) {
                             const uint64_t bd = umma_smem_desc(b_base + k * 256u, 128u, kTcSbo);
-                            tc_mma_f16(tmem + static_cast<uint32_t>(acc * kTcN), ad, bd, idesc, sb > 0 || k > 0);
+                            tc_mma_f16_ta(tmem + static_cast<uint32_t>(kTcDCol + acc * kTcDBuf + mj * kTcN),
+                                          a_col + 8u * k, bd, idesc, kb > 0 || k >= kTcMmaWarps);
                         }
                         tc_commit(smem_addr(&free_a[s]));
-                        if (sb == nsub - 1) tc_commit(smem_addr(&d_full[acc]));
+                        if (kb == nkb - 1) tc_commit(smem_addr(&d_full[acc]));
                     }
                     if (broke) break;
                 }
@@ -529,40 +597,29 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                                         static_cast<uint32_t>((last / kTcStages) & 1));
             }
         }
-    } else {
-        // ---------------- converters (+ epilogue on the first four warps)
-        // Abort checks are warp-uniform: the loops below hold warp-wide votes.
+    } else if (warp >= kTcBWarp0) {
+        // ---------------- B builders: per operand stage, x_bi's columns bc.. of the
+        // K-block as hi (row bi) and lo (row 8 + bi) f16 planes of x * 2^p; zeros
+        // past the panel or for bi >= m.
         auto warp_aborted = [&]() { return __any_sync(0xFFFFFFFFu, tc_aborted(&s_abort)); };
-        // B work of this thread: activation row bi, kTcBValsPerThread consecutive
-        // columns from bc; the pre-scale 2^p as two normal f32 factors.
-        const int bi = tid & 7;
-        const int bc = (tid >> 3) * kTcBValsPerThread;
+        constexpr int V = kTcBValsPerThread;
+        const int bt = tid - kTcBWarp0 * 32;
+        const int bi = bt & 7;
+        const int bc = (bt >> 3) * V;  // first column within the K-block (whole K-cores)
         const int pb = s_p[bi];
         const float pfa = pow2f_normal(pb / 2), pfb = pow2f_normal(pb - pb / 2);
         int64_t u = 0, e = 0;
-        int tile_seq = 0;
         for (int p = 0; p < a.panels && !warp_aborted(); ++p) {
             const int pc = panel_cols_of(p);
             const int nkb = nkb_of(p);
-            const int kglob0 = p * (a.panel_cols / kTcKb);  // first global K-block of the panel
-            for (int t = 0; t < n_tiles && !warp_aborted(); ++t, ++tile_seq) {
-                const TcTile tl = tc_tile(r0, r1, t);
-                // Scale-table row of each owned 8-row group.
-                int sf_row[kTcGroupsPerWarp];
-#pragma unroll
-                for (int g = 0; g < kTcGroupsPerWarp; ++g) {
-                    const int64_t grow = tl.row0 + (warp * kTcGroupsPerWarp + g) * 8;
-                    const int64_t growc = grow < r1 ? grow : r1 - 1;  // groups past r1 are never read back
-                    sf_row[g] = static_cast<int>((growc >> 7) - rb0) * static_cast<int>(gcols);
-                }
-                bool broke = false;
-                for (int kb = 0; kb < nkb && !broke; ++kb)
-                for (int sub = 0; sub < kTcSub; ++sub, ++u) {
+            bool broke = false;
+            for (int t = 0; t < n_tiles && !broke && !warp_aborted(); ++t) {
+                for (int kb = 0; kb < nkb; ++kb, ++u) {
                     const int k2 = kb % kTcKbPerStage;
                     const int se = static_cast<int>(e % kTcEStages);
                     const int s = static_cast<int>(u % kTcStages);
                     bool ok = true;
-                    if (k2 == 0 && sub == 0)
+                    if (k2 == 0)
                         ok = mbar_wait_bounded<kTcSleep>(smem_addr(&full_e[se]), static_cast<uint32_t>((e / kTcEStages) & 1));
                     if (ok && u >= kTcStages)
                         ok = mbar_wait_bounded<kTcSleep>(smem_addr(&free_a[s]), static_cast<uint32_t>((u / kTcStages - 1) & 1));
@@ -571,29 +628,103 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                         broke = true;
                         break;
                     }
+                    const float *xs = reinterpret_cast<const float *>(sE + se * kTcEStageBytes + kTcKbPerStage * kTcETileBytes) +
+                                      k2 * kTcKb;
+                    uint8_t *btile = sB + s * kTcBTileBytes;
+                    uint32_t hw[V / 2], lw[V / 2];
+#pragma unroll
+                    for (int q = 0; q < V / 2; ++q) hw[q] = lw[q] = 0u;
+                    if (bi < m && kb * kTcKb + bc < pc) {
+                        float vv[V];
+#pragma unroll
+                        for (int q = 0; q < V; q += 4) {
+                            const float4 v4 = *reinterpret_cast<const float4 *>(xs + bi * kTcXCols + bc + q);
+                            vv[q] = v4.x;
+                            vv[q + 1] = v4.y;
+                            vv[q + 2] = v4.z;
+                            vv[q + 3] = v4.w;
+                        }
+#pragma unroll
+                        for (int q = 0; q < V / 2; ++q) {
+                            const float s0 = vv[2 * q] * pfa * pfb, s1 = vv[2 * q + 1] * pfa * pfb;
+                            const __half2 hh = __floats2half2_rn(s0, s1);
+                            const float2 hb = __half22float2(hh);
+                            const __half2 ll = __floats2half2_rn(s0 - hb.x, s1 - hb.y);
+                            hw[q] = *reinterpret_cast<const uint32_t *>(&hh);
+                            lw[q] = *reinterpret_cast<const uint32_t *>(&ll);
+                        }
+                    }
+                    // K-core bc / 8 + c holds columns 8c..8c+7 of this thread's run
+#pragma unroll
+                    for (int c = 0; c < V / 8; ++c) {
+                        uint8_t *bh = btile + ((bc >> 3) + c) * 128 + bi * 16;
+                        *reinterpret_cast<uint4 *>(bh) = make_uint4(hw[4 * c], hw[4 * c + 1], hw[4 * c + 2], hw[4 * c + 3]);
+                        *reinterpret_cast<uint4 *>(bh + kTcSbo) =
+                            make_uint4(lw[4 * c], lw[4 * c + 1], lw[4 * c + 2], lw[4 * c + 3]);
+                    }
+                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // generic stores -> the MMA
+                    __syncwarp();
+                    const bool stage_done = k2 == kTcKbPerStage - 1 || kb == nkb - 1;
+                    if (lane == 0) {
+                        mbar_arrive(smem_addr(&conv_a[s]));
+                        if (stage_done) mbar_arrive(smem_addr(&empty_e[se]));
+                    }
+                    if (stage_done) ++e;
+                }
+            }
+            if (broke) break;
+        }
+    } else {
+        // ---------------- converters (+ epilogue on the first four warps)
+        // Abort checks are warp-uniform: the loops below hold warp-wide votes.
+        auto warp_aborted = [&]() { return __any_sync(0xFFFFFFFFu, tc_aborted(&s_abort)); };
+        // A work of this thread: tile row tr_a (TMEM lane), K slice kq.
+        const int kq = warp >> 2;
+        const int tr_a = (warp & 3) * 32 + lane;
+        const uint32_t a_taddr = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16) + static_cast<uint32_t>(kq * (kTcKW / 2));
+        int64_t u = 0, e = 0;
+        int tile_seq = 0;
+        for (int p = 0; p < a.panels && !warp_aborted(); ++p) {
+            const int pc = panel_cols_of(p);
+            const int nkb = nkb_of(p);
+            const int kglob0 = p * (a.panel_cols / kTcKb);  // first global K-block of the panel
+            for (int t = 0; t < n_tiles && !warp_aborted(); ++t, ++tile_seq) {
+                const TcTile tl = tc_tile(r0, r1, t);
+                // Scale-table row of this thread's tile row (rows past r1 use the last
+                // row's: their accumulator rows are never read).
+                const int64_t arow = tl.row0 + tr_a < r1 ? tl.row0 + tr_a : r1 - 1;
+                const int sf_row = static_cast<int>((arow >> 7) - rb0) * static_cast<int>(gcols);
+                const bool a_live = (tr_a & ~31) < tl.rows;  // warp-uniform: some row of this quarter is in the tile
+                bool broke = false;
+                for (int kb = 0; kb < nkb; ++kb, ++u) {
+                    const int k2 = kb % kTcKbPerStage;
+                    const int se = static_cast<int>(e % kTcEStages);
+                    const int s = static_cast<int>(u % kTcStages);
+                    bool ok = true;
+                    if (k2 == 0)
+                        ok = mbar_wait_bounded<kTcSleep>(smem_addr(&full_e[se]), static_cast<uint32_t>((e / kTcEStages) & 1));
+                    if (ok && u >= kTcStages)
+                        ok = mbar_wait_bounded<kTcSleep>(smem_addr(&free_a[s]), static_cast<uint32_t>((u / kTcStages - 1) & 1));
+                    if (!__all_sync(0xFFFFFFFFu, ok)) {
+                        tc_raise_abort(&s_abort);
+                        broke = true;
+                        break;
+                    }
+                    tc_fence_after();  // the MMA that read this operand stage has completed
                     const uint8_t *stg = sE + se * kTcEStageBytes;
                     const uint8_t *et = stg + k2 * kTcETileBytes;
-                    const float *xs = reinterpret_cast<const float *>(stg + kTcKbPerStage * kTcETileBytes) + k2 * kTcKb;
-                    uint8_t *at = sAB + s * kTcABStageBytes;
-                    uint8_t *btile = at + kTcATileBytes;
                     const int kglob = kglob0 + kb;
-                    // A: this warp's 8-row groups; lane = (chunk in half, row in group).
-                    // Groups wholly past the tile's rows are skipped: their A rows feed
-                    // accumulator rows that are never read.
-#pragma unroll
-                    for (int g = 0; g < kTcGroupsPerWarp; ++g) {
-                        const int G = warp * kTcGroupsPerWarp + g;
-                        if (G * 8 >= tl.rows) break;
-                        const int tr = G * 8 + (lane & 7);
-                        const __half sfh = s_sf[sf_row[g] + kglob];
+                    // A: this thread's row, K columns [kq * kTcKW, (kq + 1) * kTcKW), codes ->
+                    // f16 * S * 2^-q, stored to its TMEM lane (two f16 per column).
+                    if (a_live) {
+                        const __half sfh = s_sf[sf_row + kglob];
                         const __half2 sf2 = __halves2half2(sfh, sfh);
+                        uint32_t o[kTcChunks * 8];
 #pragma unroll
-                        for (int h = 0; h < kTcAK / 64; ++h) {
-                            const int kc = (lane >> 3) + 4 * h;        // 16-column chunk within the operand stage
-                            const int kcg = sub * (kTcAK / 16) + kc;  // ... within the K-block
-                            const uint4 q = *reinterpret_cast<const uint4 *>(et + tr * 128 + ((kcg ^ (tr & 7)) << 4));
+                        for (int c = 0; c < kTcChunks; ++c) {
+                            const int kc = kq * kTcChunks + c;  // 16-code chunk within the K-block
+                            const uint4 q = *reinterpret_cast<const uint4 *>(et + tr_a * 128 + ((kc ^ (tr_a & 7)) << 4));
                             const uint32_t wds[4] = {q.x, q.y, q.z, q.w};
-                            uint32_t o[8];
 #pragma unroll
                             for (int j = 0; j < 4; ++j) {
                                 uint32_t h01, h23;
@@ -603,50 +734,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                                     : "r"(wds[j]));
                                 const __half2 p01 = __hmul2(*reinterpret_cast<const __half2 *>(&h01), sf2);
                                 const __half2 p23 = __hmul2(*reinterpret_cast<const __half2 *>(&h23), sf2);
-                                o[2 * j] = *reinterpret_cast<const uint32_t *>(&p01);
-                                o[2 * j + 1] = *reinterpret_cast<const uint32_t *>(&p23);
+                                o[c * 8 + 2 * j] = *reinterpret_cast<const uint32_t *>(&p01);
+                                o[c * 8 + 2 * j + 1] = *reinterpret_cast<const uint32_t *>(&p23);
                             }
-                            uint8_t *dst = at + (tr >> 3) * kTcSbo + (2 * kc) * 128 + (tr & 7) * 16;
-                            *reinterpret_cast<uint4 *>(dst) = make_uint4(o[0], o[1], o[2], o[3]);
-                            *reinterpret_cast<uint4 *>(dst + 128) = make_uint4(o[4], o[5], o[6], o[7]);
                         }
+                        tc_st<kTcChunks * 8>(a_taddr + static_cast<uint32_t>(s * kTcACols), o);
+                        asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
                     }
-                    // B (all converter threads): x_bi's columns bc.. as hi (row bi) and lo
-                    // (row 8 + bi); zeros past the panel or for bi >= m.
-                    {
-                        uint32_t hw[kTcBValsPerThread / 2], lw[kTcBValsPerThread / 2];
-#pragma unroll
-                        for (int q = 0; q < kTcBValsPerThread / 2; ++q) hw[q] = lw[q] = 0u;
-                        const int bcol = sub * kTcAK + bc;  // column within the K-block
-                        if (bi < m && kb * kTcKb + bcol < pc) {
-                            float vv[kTcBValsPerThread];
-#pragma unroll
-                            for (int q = 0; q < kTcBValsPerThread; q += 2) {
-                                const float2 v2 = *reinterpret_cast<const float2 *>(xs + bi * kTcXCols + bcol + q);
-                                vv[q] = v2.x;
-                                vv[q + 1] = v2.y;
-                            }
-#pragma unroll
-                            for (int q = 0; q < kTcBValsPerThread / 2; ++q) {
-                                const float s0 = vv[2 * q] * pfa * pfb, s1 = vv[2 * q + 1] * pfa * pfb;
-                                const __half2 hh = __floats2half2_rn(s0, s1);
-                                const float2 hb = __half22float2(hh);
-                                const __half2 ll = __floats2half2_rn(s0 - hb.x, s1 - hb.y);
-                                hw[q] = *reinterpret_cast<const uint32_t *>(&hh);
-                                lw[q] = *reinterpret_cast<const uint32_t *>(&ll);
-                            }
-                        }
-                        // core column bc / 8, byte offset (bc % 8) * 2 within the 16-byte row
-                        uint8_t *bh = btile + (bc >> 3) * 128 + bi * 16 + (bc & 7) * 2;
-#pragma unroll
-                        for (int q = 0; q < kTcBValsPerThread / 2; ++q) {
-                            *reinterpret_cast<uint32_t *>(bh + 4 * q) = hw[q];
-                            *reinterpret_cast<uint32_t *>(bh + kTcSbo + 4 * q) = lw[q];
-                        }
-                    }
-                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                    tc_fence_before();  // A's tensor-memory stores -> the MMA
                     __syncwarp();
-                    const bool stage_done = sub == kTcSub - 1 && (k2 == kTcKbPerStage - 1 || kb == nkb - 1);
+                    const bool stage_done = k2 == kTcKbPerStage - 1 || kb == nkb - 1;
                     if (lane == 0) {
                         mbar_arrive(smem_addr(&conv_a[s]));
                         if (stage_done) mbar_arrive(smem_addr(&empty_e[se]));
@@ -666,7 +763,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 }
                 tc_fence_after();
                 float v[16];
-                tc_ld16(tmem + static_cast<uint32_t>(acc * kTcN) + (static_cast<uint32_t>(warp * 32) << 16), v);
+                tc_ld16(tmem + static_cast<uint32_t>(kTcDCol + acc * kTcDBuf) + (static_cast<uint32_t>(warp * 32) << 16), v);
+#pragma unroll
+                for (int c = 1; c < kTcNAcc; ++c) {
+                    float w[16];
+                    tc_ld16(tmem + static_cast<uint32_t>(kTcDCol + acc * kTcDBuf + c * kTcN) +
+                                (static_cast<uint32_t>(warp * 32) << 16),
+                            w);
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) v[j] += w[j];
+                }
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(smem_addr(&d_free[acc]));
@@ -731,13 +837,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         ga.counter = a.counter;
         ga.tokens = a.tokens;
         switch (m) {  // the cross-CTA merge is templated on the row count
-            case 2: argmax_cross_cta<2, kTcThreads>(ga, am_val, am_idx, &s_is_last); break;
-            case 3: argmax_cross_cta<3, kTcThreads>(ga, am_val, am_idx, &s_is_last); break;
-            case 4: argmax_cross_cta<4, kTcThreads>(ga, am_val, am_idx, &s_is_last); break;
-            case 5: argmax_cross_cta<5, kTcThreads>(ga, am_val, am_idx, &s_is_last); break;
-            case 6: argmax_cross_cta<6, kTcThreads>(ga, am_val, am_idx, &s_is_last); break;
-            case 7: argmax_cross_cta<7, kTcThreads>(ga, am_val, am_idx, &s_is_last); break;
-            default: argmax_cross_cta<8, kTcThreads>(ga, am_val, am_idx, &s_is_last); break;
+            case 2: argmax_cross_cta<2, kTcThreads, kTcThreads / 32>(ga, am_val, am_idx, &s_is_last); break;
+            case 3: argmax_cross_cta<3, kTcThreads, kTcThreads / 32>(ga, am_val, am_idx, &s_is_last); break;
+            case 4: argmax_cross_cta<4, kTcThreads, kTcThreads / 32>(ga, am_val, am_idx, &s_is_last); break;
+            case 5: argmax_cross_cta<5, kTcThreads, kTcThreads / 32>(ga, am_val, am_idx, &s_is_last); break;
+            case 6: argmax_cross_cta<6, kTcThreads, kTcThreads / 32>(ga, am_val, am_idx, &s_is_last); break;
+            case 7: argmax_cross_cta<7, kTcThreads, kTcThreads / 32>(ga, am_val, am_idx, &s_is_last); break;
+            default: argmax_cross_cta<8, kTcThreads, kTcThreads / 32>(ga, am_val, am_idx, &s_is_last); break;
         }
     }
 }
