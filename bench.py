@@ -72,8 +72,8 @@ def nvfp4_bytes(n_active: int, rows: int, cols: int) -> int:
 
 
 # Sources that define the streaming kernels and their launch geometry.
-KERNEL_SOURCES = ("device_common.cuh", "stream_gemv.cuh", "rowwarp_gemv.cuh", "launch.h", "abi.cu",
-                  "gemv_e4m3.cu", "gemv_bf16.cu", "nvfp4_dequant.cu")
+KERNEL_SOURCES = ("device_common.cuh", "stream_gemv.cuh", "rowwarp_gemv.cuh", "tc_gemv.cuh", "launch.h", "abi.cu",
+                  "gemv_e4m3.cu", "gemv_bf16.cu", "gemv_tc.cu", "nvfp4_dequant.cu")
 
 
 def source_hash() -> str:
@@ -300,7 +300,11 @@ def setup_fp8blk(name: str, device, argmax: bool = False):
                 bytes=fp8blk_bytes(rows, cols, m, argmax))
 
 
-def setup_nvfp4(device):
+def setup_nvfp4(device, fused: bool = True):
+    """C5 with ten rotating active-expert sets (the 64-expert pool is 301 MB, so
+    the active experts' bytes come from HBM).  fused: one launch per call
+    (in-register decode, ids and global scales on the device); otherwise the
+    dequant-to-scratch + bf16 GEMV arm, two launches per active expert."""
     import numpy as np
     import torch
     from fp8_block_scaled_fp8blk_gb300 import ops, synth
@@ -311,11 +315,19 @@ def setup_nvfp4(device):
     rng = np.random.default_rng(w["seed"] + 100)
     id_sets = [c.ids] + [rng.choice(w["n_experts"], w["n_active"], replace=False).astype(np.int32)
                          for _ in range(9)]
-    scratch = torch.empty((rows, cols), dtype=torch.int16, device=device)
     ys = [torch.empty((w["n_active"], rows), dtype=torch.float32, device=device) for _ in id_sets]
-    calls = [lambda i=i: ops.nvfp4_expert_dequant_gemv(codes, scales, c.gscale, id_sets[i], x,
-                                                       scratch, y=ys[i]) for i in range(len(id_sets))]
-    return dict(calls=calls, bytes=nvfp4_bytes(w["n_active"], rows, cols), launches=2 * w["n_active"])
+    if fused:
+        g_dev = up(c.gscale, device)
+        ids_dev = [up(np.asarray(i, dtype=np.int32), device) for i in id_sets]
+        calls = [lambda i=i: ops.nvfp4_expert_gemv(codes, scales, g_dev, ids_dev[i], x, y=ys[i])
+                 for i in range(len(id_sets))]
+        launches = 1
+    else:
+        scratch = torch.empty((rows, cols), dtype=torch.int16, device=device)
+        calls = [lambda i=i: ops.nvfp4_expert_dequant_gemv(codes, scales, c.gscale, id_sets[i], x,
+                                                           scratch, y=ys[i]) for i in range(len(id_sets))]
+        launches = 2 * w["n_active"]
+    return dict(calls=calls, bytes=nvfp4_bytes(w["n_active"], rows, cols), launches=launches)
 
 
 def measure_extra(device, stream, world, peak):
@@ -335,15 +347,21 @@ def measure_extra(device, stream, world, peak):
                      "weight_copies": st["copies"], "steps": steps,
                      "kernel": kernel_name(ops, st["m"], st["rows"], st["cols"], argmax)}
         del st
-    st = setup_nvfp4(device)
-    steps = 500
-    ms, _ = time_graphed(st["calls"], steps, 20, stream, world, device, per_graph=100)
-    us = ms * 1e3 / steps
-    gbs = st["bytes"] / (us * 1e-6) / 1e9
-    out["nvfp4_experts_6of64_2048x4096"] = {
-        "us_per_call": round(us, 3), "gbs": round(gbs, 1), "frac_of_hbm_peak": round(gbs / peak, 4),
-        "bytes_per_call": st["bytes"], "launches_per_call": st["launches"], "steps": steps,
-        "note": "algorithmic bytes exclude the 2 x 16 MiB bf16 scratch write+read per expert"}
+    for fused, name, note in (
+            (True, "nvfp4_experts_6of64_2048x4096",
+             "one launch: NVFP4 decoded in registers, expert ids and global scales on the device"),
+            (False, "nvfp4_experts_6of64_2048x4096_two_step",
+             "dequant to the reused bf16 scratch + bf16 GEMV per expert; algorithmic bytes exclude "
+             "the 2 x 16 MiB scratch write+read per expert")):
+        st = setup_nvfp4(device, fused)
+        steps = 2000 if fused else 500
+        ms, _ = time_graphed(st["calls"], steps, 20, stream, world, device, per_graph=200 if fused else 100)
+        us = ms * 1e3 / steps
+        gbs = st["bytes"] / (us * 1e-6) / 1e9
+        out[name] = {
+            "us_per_call": round(us, 3), "gbs": round(gbs, 1), "frac_of_hbm_peak": round(gbs / peak, 4),
+            "bytes_per_call": st["bytes"], "launches_per_call": st["launches"], "steps": steps, "note": note}
+        del st
     return out
 
 
@@ -541,8 +559,8 @@ def run_profile_workload(args):
     device = torch.device("cuda", 0)
     torch.cuda.set_device(device)
     ops.set_tensor_core_min_m(args.tensor_core_min_m, args.tensor_core_min_bytes)
-    if args.profile_workload == "nvfp4_experts_6of64_2048x4096":
-        st = setup_nvfp4(device)
+    if args.profile_workload.startswith("nvfp4_experts_6of64_2048x4096"):
+        st = setup_nvfp4(device, fused=not args.profile_workload.endswith("_two_step"))
     else:
         st = setup_fp8blk(args.profile_workload, device, args.profile_workload.startswith("head_argmax"))
     for i in range(args.calls):

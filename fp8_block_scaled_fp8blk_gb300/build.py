@@ -24,7 +24,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(BUILD, "libfp8blk.so")
-SOURCES = ["abi.cu", "gemv_e4m3.cu", "gemv_bf16.cu", "gemv_tc.cu", "nvfp4_dequant.cu", "noalloc.cu"]
+SOURCES = ["abi.cu", "gemv_e4m3.cu", "gemv_bf16.cu", "gemv_tc.cu", "nvfp4_dequant.cu", "nvfp4_gemv.cu", "noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -485,6 +485,32 @@ int nvfp4_expert_dequant_gemv(const uint8_t *codes, const uint8_t *scales,
     return FP8BLK_OK;
 }
 
+int nvfp4_expert_gemv(const uint8_t *codes, const uint8_t *scales, const float *gscale, int n_experts,
+                      const int32_t *ids, int n_active, const float *x, float *y, int64_t rows, int64_t cols,
+                      void *stream) {
+    if (!codes || !scales || !gscale || !ids || !x || !y || n_experts < 1) return FP8BLK_EINVAL;
+    if (n_active < 1 || n_active > 65536 || rows < 1 || cols < 256 || cols % 256 != 0) return FP8BLK_EINVAL;
+    if (rows > kMaxIndex || cols > kMaxIndex) return FP8BLK_ERANGE;
+    if (!aligned(codes, 16) || !aligned(scales, 16) || !aligned(gscale, 4) || !aligned(ids, 4) || !aligned(x, 16) ||
+        !aligned(y, 4))
+        return FP8BLK_EALIGN;
+    DeviceInfo dev;
+    if (current_device_info(&dev) != cudaSuccess) return from_cuda(cudaErrorUnknown);
+    Nvfp4Args a = {};
+    a.codes = codes;
+    a.scales = scales;
+    a.gscale = gscale;
+    a.ids = ids;
+    a.x = x;
+    a.y = y;
+    a.status = dev.status;
+    a.n_experts = n_experts;
+    a.n_active = n_active;
+    a.rows = rows;
+    a.cols = cols;
+    return from_cuda(launch_nvfp4_gemv(a, dev, static_cast<cudaStream_t>(stream)));
+}
+
 int fp8blk_set_launch_tuning(int target_stage_bytes, int ctas_per_sm, int use_pdl, int l2_prefetch,
                              int max_stages) {
     if (target_stage_bytes < 0 || ctas_per_sm < 0 || ctas_per_sm > 4 || max_stages < 0 ||

@@ -85,6 +85,26 @@ cudaError_t launch_nvfp4_dequant(const uint8_t *codes, const uint8_t *scales, fl
 // capture) make no attribute or occupancy calls.
 cudaError_t kernel_occupancy(const void *kernel, int threads, size_t smem, int *per_sm);
 
+// One-launch NVFP4 routed-expert GEMV (kernel in nvfp4_gemv.cuh, launch in
+// nvfp4_gemv.cu, which plans the panels, stages and grid itself).
+struct Nvfp4Args {
+    const uint8_t *codes;    // [n_experts, rows, cols / 2]
+    const uint8_t *scales;   // [n_experts, rows, cols / 16] e4m3
+    const float *gscale;     // [n_experts], device
+    const int32_t *ids;      // [n_active], device
+    const float *x;          // [cols]
+    float *y;                // [n_active, rows]
+    unsigned int *status;
+    int n_experts, n_active;
+    int64_t rows, cols;
+    int panels, panel_cols;  // panel_cols = cols (one panel) or 4096
+    int stage_rows;          // R rows per stage
+    int stage_bytes;         // R * (panel_cols / 2 + panel_cols / 16)
+    int stages;
+    int64_t groups;          // row groups per expert: ceil(rows / R)
+};
+cudaError_t launch_nvfp4_gemv(Nvfp4Args a, const DeviceInfo &dev, cudaStream_t stream);
+
 // Dynamic shared memory of a planned launch.
 inline size_t plan_smem_bytes(const Plan &p) {
     if (p.kind == kTensorCoreKernel) return kTcSmemBytes;

@@ -1,0 +1,62 @@
+// nvfp4_gemv.cu -- plan and launch of the one-launch NVFP4 routed-expert GEMV
+// (nvfp4_gemv.cuh).
+#include "launch.h"
+#include "nvfp4_gemv.cuh"
+
+#ifndef NV_STAGE_TARGET
+#define NV_STAGE_TARGET 16384
+#endif
+#ifndef NV_SHRINK
+#define NV_SHRINK 1
+#endif
+
+namespace fp8blk {
+
+cudaError_t launch_nvfp4_gemv(Nvfp4Args a, const DeviceInfo &dev, cudaStream_t stream) {
+    a.panels = static_cast<int>((a.cols + kNvMaxPanel - 1) / kNvMaxPanel);
+    a.panel_cols = a.panels == 1 ? static_cast<int>(a.cols) : kNvMaxPanel;
+    const int row_bytes = a.panel_cols / 2 + a.panel_cols / 16;
+    // Stages of about 8 KiB (R rows), fewer rows while there are fewer row
+    // groups than warps; as many stages as two CTAs per SM leave room for.
+    const int ctas_per_sm = 2;
+    int rw = 1;
+    while (rw < 8 && 2 * rw * row_bytes <= NV_STAGE_TARGET) rw *= 2;
+    const int64_t warps = static_cast<int64_t>(dev.sms) * ctas_per_sm * kNvWarps;
+    while (NV_SHRINK && rw > 1 && (a.rows + rw - 1) / rw * a.n_active < warps) rw /= 2;
+    a.stage_rows = rw;
+    a.stage_bytes = rw * row_bytes;
+    a.groups = (a.rows + rw - 1) / rw;
+    const int x_bytes = a.panels == 1 ? kNvXSmemBytes : 0;  // x staged once per CTA
+    int per_cta = dev.smem_per_sm / ctas_per_sm - 1024 - kStaticSmemReserve;
+    const int block_cap = dev.smem_per_block - kStaticSmemReserve;
+    if (per_cta > block_cap) per_cta = block_cap;
+    const int per_warp = (per_cta - x_bytes) / kNvWarps;
+    int stages = per_warp / a.stage_bytes;
+    if (stages > kMaxStages) stages = kMaxStages;
+    if (stages < 2) return cudaErrorInvalidConfiguration;
+    a.stages = stages;
+    const size_t smem = static_cast<size_t>(x_bytes) + static_cast<size_t>(kNvWarps) * stages * a.stage_bytes;
+    int per_sm = 0;
+    cudaError_t err = kernel_occupancy(reinterpret_cast<const void *>(nvfp4_gemv_kernel), kNvThreads, smem, &per_sm);
+    if (err != cudaSuccess) return err;
+    if (per_sm < 1) return cudaErrorInvalidConfiguration;
+    const int64_t total_groups = a.groups * a.n_active;
+    int64_t grid = (total_groups + kNvWarps - 1) / kNvWarps;
+    const int64_t cap = static_cast<int64_t>(dev.sms) * (per_sm < ctas_per_sm ? per_sm : ctas_per_sm);
+    if (grid > cap) grid = cap;
+    if (grid > kMaxGrid) grid = kMaxGrid;
+    if (grid < 1) grid = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(grid));
+    cfg.blockDim = dim3(kNvThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = tuning().use_pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, nvfp4_gemv_kernel, a);
+}
+
+}  // namespace fp8blk

@@ -71,7 +71,7 @@
 #define TC_B_WARPS 4
 #endif
 #ifndef TC_MMA_SLEEP
-#define TC_MMA_SLEEP 0
+#define TC_MMA_SLEEP 1
 #endif
 
 namespace fp8blk {

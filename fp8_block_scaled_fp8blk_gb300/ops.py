@@ -50,6 +50,8 @@ _lib.nvfp4_expert_dequant.restype = _INT
 _lib.nvfp4_expert_dequant.argtypes = [_P, _P, _P, _INT, _INT, _P, _I64, _I64, _P]
 _lib.nvfp4_expert_dequant_gemv.restype = _INT
 _lib.nvfp4_expert_dequant_gemv.argtypes = [_P, _P, _P, _INT, _P, _INT, _P, _P, _P, _I64, _I64, _P]
+_lib.nvfp4_expert_gemv.restype = _INT
+_lib.nvfp4_expert_gemv.argtypes = [_P, _P, _P, _INT, _P, _INT, _P, _P, _I64, _I64, _P]
 _lib.fp8blk_set_launch_tuning.restype = _INT
 _lib.fp8blk_set_launch_tuning.argtypes = [_INT, _INT, _INT, _INT, _INT]
 _lib.fp8blk_set_m1_kernel.restype = _INT
@@ -64,6 +66,7 @@ _lib.fp8blk_device_status.argtypes = [ctypes.POINTER(ctypes.c_uint32), _INT]
 # Return codes (include/fp8blk.h)
 OK, EINVAL, EALIGN, ESCALE, EWS, ECUDA, ERANGE = 0, 1, 2, 3, 4, 5, 6
 STATUS_WAIT_TIMEOUT = 1
+STATUS_BAD_EXPERT = 2
 
 
 class Fp8BlkError(RuntimeError):
@@ -223,6 +226,22 @@ def nvfp4_expert_dequant_gemv(codes: torch.Tensor, scales: torch.Tensor, gscale,
                                           ids_h.ctypes.data, ids_h.size, _ptr(x), _ptr(y),
                                           _ptr(scratch), rows, cols, _stream(x)),
            "nvfp4_expert_dequant_gemv")
+    return y
+
+
+def nvfp4_expert_gemv(codes: torch.Tensor, scales: torch.Tensor, gscale: torch.Tensor, ids: torch.Tensor,
+                      x: torch.Tensor, y: torch.Tensor | None = None) -> torch.Tensor:
+    """y [n_active, rows] = W(ids[k]) x in one launch, NVFP4 decoded in registers;
+    `gscale` (f32 [n_experts]) and `ids` (int32 [n_active]) stay on the device."""
+    n_experts, rows, half = codes.shape
+    cols = 2 * half
+    if gscale.dtype != torch.float32 or ids.dtype != torch.int32:
+        raise TypeError("gscale must be float32 and ids int32 device tensors")
+    n_active = ids.numel()
+    if y is None:
+        y = torch.empty((n_active, rows), dtype=torch.float32, device=x.device)
+    _check(_lib.nvfp4_expert_gemv(_ptr(codes), _ptr(scales), _ptr(gscale), n_experts, _ptr(ids), n_active,
+                                  _ptr(x), _ptr(y), rows, cols, _stream(x)), "nvfp4_expert_gemv")
     return y
 
 

@@ -43,6 +43,9 @@ extern "C" {
 /* Bits of the device status word (see fp8blk_device_status). */
 #define FP8BLK_STATUS_WAIT_TIMEOUT 1u /* a kernel gave up waiting for a weight tile (bounded
                                          wait, about one second); its outputs are invalid */
+#define FP8BLK_STATUS_BAD_EXPERT 2u   /* nvfp4_expert_gemv met a device-side expert id outside
+                                         [0, n_experts) or a global scale that is not a power
+                                         of two in [2^-100, 2^100]; that slot's outputs are NaN */
 
 /* Version of this ABI; bumped on any incompatible change. */
 int fp8blk_abi_version(void);
@@ -197,6 +200,32 @@ int nvfp4_expert_dequant_gemv(const uint8_t *codes, const uint8_t *scales,
                               const float *gscale_host, int n_experts, const int32_t *ids_host,
                               int n_active, const float *x, float *y, uint16_t *bf16_scratch,
                               int64_t rows, int64_t cols, void *stream);
+
+/*
+ * nvfp4_expert_gemv -- y[k] = W(ids[k]) x for k < n_active in ONE launch,
+ * decoding the NVFP4 weights in registers (no bf16 scratch):
+ *   y[k][r] = sum_c bf16(e2m1(q[e][r][c]) * e4m3(s[e][r][c/16]) * g[e]) * x[c],
+ *   e = ids[k]; every product is exact, so the weights take the same values
+ *   as nvfp4_expert_dequant writes; the sum is in f32.
+ * Source: "Module dsv4_gpu" page, module header (routed experts stay NVFP4 as
+ * stored; one-launch-per-projection indirect expert dispatch) and enum
+ * ExpertArm.  The router's output stays on the device: ids and global scales
+ * are read by the kernel, so the host checks neither.
+ *   codes, scales as nvfp4_expert_dequant, but scales 16-byte aligned
+ *   gscale       DEVICE, f32 [n_experts], 4-byte aligned: per-expert global
+ *                scale, a power of two in [2^-100, 2^100]
+ *   ids          DEVICE, int32 [n_active], 4-byte aligned; repeats allowed
+ *   n_active     1 .. 65536
+ *   x            device, f32 [cols], 16-byte aligned
+ *   y            device, f32 [n_active, rows], 4-byte aligned
+ *   cols         a multiple of 256 (so every scale row starts on 16 bytes).
+ * An id outside [0, n_experts) or an unusable global scale sets
+ * FP8BLK_STATUS_BAD_EXPERT in the device status word and makes y[k] NaN.
+ * Errors: EINVAL, EALIGN, ERANGE, ECUDA.
+ */
+int nvfp4_expert_gemv(const uint8_t *codes, const uint8_t *scales, const float *gscale, int n_experts,
+                      const int32_t *ids, int n_active, const float *x, float *y, int64_t rows, int64_t cols,
+                      void *stream);
 
 /*
  * fp8blk_set_launch_tuning -- process-wide launch-shape knobs for the

@@ -71,3 +71,68 @@ def test_expert_dequant_gemv_ragged(ops):
     ref, a, _ = oracle.nvfp4_expert_dequant_gemv(case.codes, case.scales, case.gscale, case.ids,
                                                  case.x, nthreads=8)
     assert_close(y, ref, a, "nvfp4 ragged")
+
+
+# ---- one-launch expert GEMV, NVFP4 decoded in registers, ids on the device
+
+def fused(ops, case, ids=None, gscale=None):
+    ids = case.ids if ids is None else ids
+    g = case.gscale if gscale is None else gscale
+    y = ops.nvfp4_expert_gemv(to_dev(case.codes), to_dev(case.scales), to_dev(np.asarray(g, dtype=np.float32)),
+                              to_dev(np.asarray(ids, dtype=np.int32)), to_dev(case.x))
+    torch.cuda.synchronize()
+    return y.cpu().numpy()
+
+
+def test_fused_expert_gemv_full_config(ops, c5):
+    y = fused(ops, c5)
+    ref, a, _ = oracle.nvfp4_expert_dequant_gemv(c5.codes, c5.scales, c5.gscale, c5.ids, c5.x, nthreads=16)
+    assert_close(y, ref, a, "fused nvfp4 C5")
+
+
+@pytest.mark.parametrize("n_experts,rows,cols,n_active", [(3, 1, 256, 1), (4, 7, 512, 2), (8, 129, 4096, 3),
+                                                          (5, 1000, 1280, 5), (6, 130, 4352, 4),
+                                                          (4, 65, 8192, 4), (70, 64, 256, 70)])
+def test_fused_expert_gemv_ragged(ops, n_experts, rows, cols, n_active):
+    """Ragged rows, one and several column panels (4352 = 4096 + 256), every
+    expert active, more slots than one row group each."""
+    case = synth.nvfp4_case(n_experts, rows, cols, n_active, seed=rows * 31 + cols + n_active)
+    y = fused(ops, case)
+    ref, a, _ = oracle.nvfp4_expert_dequant_gemv(case.codes, case.scales, case.gscale, case.ids, case.x, nthreads=8)
+    assert_close(y, ref, a, f"fused nvfp4 {n_experts}x{rows}x{cols} k={n_active}")
+
+
+def test_fused_expert_gemv_repeated_ids_and_scales(ops):
+    """Repeated ids are allowed on the device path; per-expert global scales
+    other than 2^-4 (any power of two) scale the result exactly."""
+    case = synth.nvfp4_case(4, 300, 1024, 3, seed=55)
+    ids = np.array([2, 0, 2], dtype=np.int32)
+    g = np.array([2.0 ** -4, 2.0 ** 3, 2.0 ** -30, 1.0], dtype=np.float32)
+    y = fused(ops, case, ids=ids, gscale=g)
+    assert np.array_equal(y[0], y[2])
+    ref, a, _ = oracle.nvfp4_expert_dequant_gemv(case.codes, case.scales, g, ids[:2], case.x, nthreads=8)
+    assert_close(y[:2], ref, a, "fused nvfp4 scales")
+
+
+def test_fused_expert_gemv_bad_expert_is_nan_and_flagged(ops):
+    case = synth.nvfp4_case(4, 200, 512, 3, seed=56)
+    assert ops.fp8blk_device_status(clear=True) == 0
+    g = np.array([2.0 ** -4, 0.75, 2.0 ** -4, 2.0 ** -4], dtype=np.float32)  # expert 1: not a power of two
+    y = fused(ops, case, ids=np.array([3, 9, 1], dtype=np.int32), gscale=g)  # 9: out of range
+    assert np.isnan(y[1]).all() and np.isnan(y[2]).all()
+    ref, a, _ = oracle.nvfp4_expert_dequant_gemv(case.codes, case.scales, g, np.array([3], dtype=np.int32), case.x)
+    assert_close(y[:1], ref, a, "good slot next to bad ones")
+    assert ops.fp8blk_device_status(clear=True) == ops.STATUS_BAD_EXPERT
+    assert ops.fp8blk_device_status() == 0
+
+
+def test_fused_matches_two_step_path(ops, c5):
+    """Both arms use the same bf16 weight values; their sums agree within the
+    GEMV tolerance of each other."""
+    codes, scales, x = to_dev(c5.codes), to_dev(c5.scales), to_dev(c5.x)
+    rows, cols = c5.codes.shape[1], 2 * c5.codes.shape[2]
+    scratch = torch.empty((rows, cols), dtype=torch.int16, device="cuda:0")
+    y2 = ops.nvfp4_expert_dequant_gemv(codes, scales, c5.gscale, c5.ids, x, scratch).cpu().numpy()
+    y1 = fused(ops, c5)
+    _, a, _ = oracle.nvfp4_expert_dequant_gemv(c5.codes, c5.scales, c5.gscale, c5.ids, c5.x, nthreads=16)
+    assert np.all(np.abs(y1.astype(np.float64) - y2) <= 2 * (1e-5 * a + 1e-6))
