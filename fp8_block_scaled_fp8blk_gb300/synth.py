@@ -30,6 +30,16 @@ WORKLOADS = {
     "verify_16384x4096_m8": dict(rows=16384, cols=4096, m=8, seed=3),
 }
 NVFP4_WORKLOAD = dict(n_experts=64, rows=2048, cols=4096, n_active=6, seed=4)
+# The MTP block's routed experts (OCP MXFP4), same expert geometry as the trunk's.
+MXFP4_WORKLOAD = dict(n_experts=64, rows=2048, cols=4096, n_active=6, seed=5)
+
+
+@dataclass
+class Mxfp4Case:
+    codes: np.ndarray    # uint8 [n_experts, rows, cols/2], column 2j in the low nibble
+    scales: np.ndarray   # uint8 e8m0 [n_experts, rows, cols/32]
+    ids: np.ndarray      # int32 [n_active]
+    x: np.ndarray        # float32 [cols]
 
 
 @dataclass
@@ -86,3 +96,13 @@ def nvfp4_case(n_experts: int, rows: int, cols: int, n_active: int, seed: int,
     ids = rng.choice(n_experts, n_active, replace=False).astype(np.int32)
     x = rng.standard_normal(cols, dtype=np.float32)
     return Nvfp4Case(codes, scales, g, ids, x)
+
+
+def mxfp4_case(n_experts: int, rows: int, cols: int, n_active: int, seed: int) -> Mxfp4Case:
+    """e2m1 codes uniform over all 16; e8m0 block scales 2^[-8, 0] (codes 119..127)."""
+    rng = np.random.default_rng(seed)
+    codes = rng.integers(0, 256, size=(n_experts, rows, cols // 2), dtype=np.uint8)
+    scales = e8m0_codes(rng, (n_experts, rows, cols // 32))
+    ids = rng.choice(n_experts, n_active, replace=False).astype(np.int32)
+    x = rng.standard_normal(cols, dtype=np.float32)
+    return Mxfp4Case(codes, scales, ids, x)

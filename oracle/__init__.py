@@ -75,6 +75,9 @@ def _load():
         lib.oracle_nvfp4_expert_dequant_gemv.restype = ctypes.c_int
         lib.oracle_nvfp4_expert_dequant_gemv.argtypes = [P, P, P, ctypes.c_int, P, ctypes.c_int,
                                                          P, P, P, P, I64, I64, ctypes.c_int]
+        lib.oracle_mxfp4_expert_gemv.restype = ctypes.c_int
+        lib.oracle_mxfp4_expert_gemv.argtypes = [P, P, ctypes.c_int, P, ctypes.c_int, P, P, P, I64, I64,
+                                                 ctypes.c_int]
         _lib = lib
         return lib
 
@@ -213,3 +216,25 @@ def nvfp4_expert_dequant_gemv(codes: np.ndarray, scales: np.ndarray, gscale: np.
     if rc != 0:
         raise OracleError(f"oracle_nvfp4_expert_dequant_gemv failed ({rc})")
     return y, a, scratch
+
+
+def mxfp4_expert_gemv(codes: np.ndarray, scales: np.ndarray, ids: np.ndarray, x: np.ndarray,
+                      nthreads: int = 1) -> tuple[np.ndarray, np.ndarray]:
+    """OCP MXFP4 experts: (y [n_active, rows], sum|w x| [n_active, rows]) with
+    y[k][r] = sum_c e2m1(codes[ids[k]][r][c]) * 2^(scales[ids[k]][r][c/32] - 127) * x[c]."""
+    codes = np.ascontiguousarray(codes, dtype=np.uint8)
+    scales = np.ascontiguousarray(scales, dtype=np.uint8)
+    ids = np.ascontiguousarray(ids, dtype=np.int32)
+    x = np.ascontiguousarray(x, dtype=np.float32).ravel()
+    n_experts, rows, half = codes.shape
+    cols = 2 * half
+    assert scales.shape == (n_experts, rows, cols // 32) and x.size == cols
+    y = np.zeros((ids.size, rows), dtype=np.float64)
+    a = np.zeros((ids.size, rows), dtype=np.float64)
+    rc = _load().oracle_mxfp4_expert_gemv(_ptr(codes), _ptr(scales), n_experts, _ptr(ids), ids.size, _ptr(x),
+                                          _ptr(y), _ptr(a), rows, cols, nthreads)
+    if rc == -4:
+        raise OracleError("expert id out of range")
+    if rc != 0:
+        raise OracleError(f"oracle_mxfp4_expert_gemv failed ({rc})")
+    return y, a

@@ -31,6 +31,10 @@
  *   - scale block (i, j) covers rows [128i, 128i+128) x cols [128j, 128j+128).
  *   - NVFP4: two codes per byte, element 2j in the low nibble; one e4m3 scale
  *     per 16 consecutive columns of a row; one f32 global scale per expert.
+ *   - MXFP4 (OCP MX, the MTP block's routed experts per [dsv4_gpu]
+ *     ExpertKind): the same e2m1 code layout; one e8m0 scale per 32
+ *     consecutive columns of a row, a weight is e2m1 * 2^(s-127); scale 0xFF
+ *     is the MX NaN and makes its block's weights NaN; no global scale.
  *   - activations x are used as f32 (never rounded to bf16).
  *
  * Build: gcc -O2 -fPIC -shared -ffp-contract=off fp8blk_oracle.c -lm -lpthread
@@ -379,5 +383,74 @@ int oracle_nvfp4_expert_dequant_gemv(const uint8_t *codes, const uint8_t *scales
             memcpy(scratch_out, b, (size_t)(rows * cols) * sizeof(uint16_t));
     }
     free(b);
+    return rc;
+}
+
+/* ------------------------------------------------------------------ */
+/* MXFP4 routed experts: y[k][r] = sum_c e2m1(q[e][r][c]) * 2^(s[e][r][c/32]-127) * x[c],  */
+/* e = ids[k] (repeats allowed), each term in double, summed sequentially.  */
+/* ------------------------------------------------------------------ */
+
+typedef struct {
+    row_range range;
+    const uint8_t *codes;   /* [rows, cols/2] of one expert */
+    const uint8_t *scales;  /* [rows, cols/32] e8m0 of one expert */
+    const float *x;         /* [cols] */
+    double *y;              /* [rows] */
+    double *abs_sum;        /* [rows], may be NULL */
+    const double *e2m1;     /* 16-entry table */
+    int64_t rows, cols;
+} mx_job;
+
+static void *mx_rows(void *arg) {
+    const mx_job *j = (const mx_job *)arg;
+    for (int64_t r = j->range.r0; r < j->range.r1; ++r) {
+        const uint8_t *crow = j->codes + r * (j->cols / 2);
+        const uint8_t *srow = j->scales + r * (j->cols / 32);
+        double acc = 0.0, aacc = 0.0;
+        for (int64_t c = 0; c < j->cols; ++c) {
+            const unsigned byte = crow[c / 2];
+            const unsigned nib = (c % 2 == 0) ? (byte & 15u) : (byte >> 4);
+            const unsigned sc = srow[c / 32];
+            const double scale = sc == 0xFFu ? NAN : ldexp(1.0, (int)sc - 127);
+            const double t = j->e2m1[nib] * scale * (double)j->x[c];
+            acc += t;
+            aacc += fabs(t);
+        }
+        j->y[r] = acc;
+        if (j->abs_sum) j->abs_sum[r] = aacc;
+    }
+    return NULL;
+}
+
+/* Returns 0 on success, -2 on a resource failure, -3 on bad sizes, -4 on an
+ * expert id outside [0, n_experts). */
+int oracle_mxfp4_expert_gemv(const uint8_t *codes, const uint8_t *scales, int n_experts,
+                             const int32_t *ids, int n_active, const float *x, double *y,
+                             double *abs_sum, int64_t rows, int64_t cols, int nthreads) {
+    double e2m1[16];
+    if (rows < 0 || cols < 0 || (cols % 32) != 0 || n_active < 0) return -3;
+    for (int k = 0; k < n_active; ++k)
+        if (ids[k] < 0 || ids[k] >= n_experts) return -4;
+    oracle_e2m1_table(e2m1);
+    if (nthreads < 1) nthreads = 1;
+    mx_job *jobs = (mx_job *)calloc((size_t)nthreads, sizeof(mx_job));
+    if (!jobs) return -2;
+    int rc = 0;
+    for (int k = 0; k < n_active && rc == 0; ++k) {
+        const int64_t e = ids[k];
+        for (int t = 0; t < nthreads; ++t) {
+            jobs[t].codes = codes + e * rows * (cols / 2);
+            jobs[t].scales = scales + e * rows * (cols / 32);
+            jobs[t].x = x;
+            jobs[t].y = y + (int64_t)k * rows;
+            jobs[t].abs_sum = abs_sum ? abs_sum + (int64_t)k * rows : NULL;
+            jobs[t].e2m1 = e2m1;
+            jobs[t].rows = rows;
+            jobs[t].cols = cols;
+        }
+        rc = run_rows(mx_rows, jobs, sizeof(mx_job), rows, nthreads);
+    }
+    free(jobs);
     return rc;
 }

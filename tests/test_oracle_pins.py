@@ -355,3 +355,69 @@ def test_nvfp4_expert_rejects_bad_ids():
         with pytest.raises(oracle.OracleError):
             oracle.nvfp4_expert_dequant_gemv(case.codes, case.scales, case.gscale,
                                              np.array(ids, dtype=np.int32), case.x)
+
+
+# ------------------------------------------------------------------ MXFP4 experts
+def _mxfp4_decode_numpy(codes, scales, block=32, low_first=True):
+    """Independent decode: golden OCP e2m1 values, torch's e8m0 decoder, the
+    documented layout (column 2j in the low nibble, one scale per 32 columns).
+    `block` / `low_first` exist only so the teeth below can break the layout."""
+    e2m1 = _golden_format_values()["e2m1"]
+    t = np.array([e2m1[n] for n in range(16)], dtype=np.float64)
+    e8 = torch_e8m0_table()
+    lo, hi = codes & 15, codes >> 4
+    nib = np.stack([lo, hi] if low_first else [hi, lo], axis=-1).reshape(codes.shape[:-1] + (2 * codes.shape[-1],))
+    s = np.repeat(e8[scales].astype(np.float64), block, axis=-1)[..., : nib.shape[-1]]
+    return t[nib] * s
+
+
+def test_mxfp4_one_hot_reproduces_each_weight():
+    e2m1 = _golden_format_values()["e2m1"]
+    e8 = torch_e8m0_table()
+    s_codes = [0, 1, 100, 119, 127, 128, 200, 254]
+    rows, cols = len(s_codes), 64
+    codes = np.zeros((1, rows, cols // 2), dtype=np.uint8)
+    for j in range(cols // 2):  # nibbles 0..15 in column order, twice per row
+        codes[0, :, j] = ((2 * j) % 16) | (((2 * j + 1) % 16) << 4)
+    scales = np.array([[s, (s + 7) % 255] for s in s_codes], dtype=np.uint8)[None]
+    for c in range(cols):
+        x = np.zeros(cols, dtype=np.float32)
+        x[c] = 1.0
+        y, _ = oracle.mxfp4_expert_gemv(codes, scales, np.array([0], dtype=np.int32), x)
+        for r in range(rows):
+            want = e2m1[c % 16] * float(e8[scales[0, r, c // 32]])
+            assert float(y[0, r]) == want, (r, c)  # sums start at +0: the sign of a zero is not graded
+
+
+def test_mxfp4_matches_independent_numpy_decode_and_layout_teeth():
+    case = synth.mxfp4_case(n_experts=5, rows=37, cols=256, n_active=3, seed=11)
+    y, a = oracle.mxfp4_expert_gemv(case.codes, case.scales, case.ids, case.x)
+    x = case.x.astype(np.float64)
+    for k, e in enumerate(case.ids):
+        w = _mxfp4_decode_numpy(case.codes[e], case.scales[e])
+        np.testing.assert_allclose(a[k], np.abs(w) @ np.abs(x), rtol=1e-12)
+        assert np.all(np.abs(y[k] - w @ x) <= 1e-12 * a[k])
+        # teeth: indexing the 32-column scales by c / 16, or taking the high nibble
+        # first, gives other numbers
+        sc = case.scales[e]
+        by16 = sc[:, np.minimum(np.arange(256) // 16, sc.shape[1] - 1)]
+        wrong_scale = _mxfp4_decode_numpy(case.codes[e], by16, block=1)
+        wrong_nibble = _mxfp4_decode_numpy(case.codes[e], sc, low_first=False)
+        for wrong in (wrong_scale, wrong_nibble):
+            assert np.max(np.abs(y[k] - wrong @ x)) > 1e-6 * np.max(a[k])
+
+
+def test_mxfp4_scale_ff_is_nan_for_its_row_only():
+    case = synth.mxfp4_case(n_experts=2, rows=6, cols=64, n_active=2, seed=12)
+    case.scales[case.ids[0], 3, 1] = 0xFF
+    y, _ = oracle.mxfp4_expert_gemv(case.codes, case.scales, case.ids, case.x)
+    assert np.isnan(y[0, 3]) and not np.isnan(np.delete(y[0], 3)).any() and not np.isnan(y[1]).any()
+
+
+def test_mxfp4_ids_repeat_allowed_and_range_checked():
+    case = synth.mxfp4_case(n_experts=3, rows=4, cols=32, n_active=2, seed=13)
+    y, _ = oracle.mxfp4_expert_gemv(case.codes, case.scales, np.array([1, 1], dtype=np.int32), case.x)
+    assert np.array_equal(y[0], y[1])
+    for ids in ([3], [-1]):
+        with pytest.raises(oracle.OracleError):
+            oracle.mxfp4_expert_gemv(case.codes, case.scales, np.array(ids, dtype=np.int32), case.x)
