@@ -330,6 +330,29 @@ def setup_nvfp4(device, fused: bool = True):
     return dict(calls=calls, bytes=nvfp4_bytes(w["n_active"], rows, cols), launches=launches)
 
 
+def mxfp4_bytes(n_active: int, rows: int, cols: int) -> int:
+    """Algorithmic bytes of one MXFP4 expert call: codes + e8m0 scales of the
+    active experts, x, y."""
+    return n_active * (rows * cols // 2 + rows * cols // 32) + 4 * cols + 4 * n_active * rows
+
+
+def setup_mxfp4(device):
+    """The MTP block's OCP MXFP4 experts, C5 geometry, ten rotating active sets."""
+    import numpy as np
+    import torch
+    from fp8_block_scaled_fp8blk_gb300 import ops, synth
+    w = synth.MXFP4_WORKLOAD
+    c = synth.mxfp4_case(w["n_experts"], w["rows"], w["cols"], w["n_active"], w["seed"])
+    codes, scales, x = up(c.codes, device), up(c.scales, device), up(c.x, device)
+    rng = np.random.default_rng(w["seed"] + 100)
+    id_sets = [c.ids] + [rng.choice(w["n_experts"], w["n_active"], replace=False).astype(np.int32)
+                         for _ in range(9)]
+    ids_dev = [up(np.asarray(i, dtype=np.int32), device) for i in id_sets]
+    ys = [torch.empty((w["n_active"], w["rows"]), dtype=torch.float32, device=device) for _ in id_sets]
+    calls = [lambda i=i: ops.mxfp4_expert_gemv(codes, scales, ids_dev[i], x, y=ys[i]) for i in range(len(id_sets))]
+    return dict(calls=calls, bytes=mxfp4_bytes(w["n_active"], w["rows"], w["cols"]), launches=1)
+
+
 def measure_extra(device, stream, world, peak):
     """The other workloads of the path, measured the same way (one JSON line)."""
     from fp8_block_scaled_fp8blk_gb300 import ops
@@ -362,6 +385,14 @@ def measure_extra(device, stream, world, peak):
             "us_per_call": round(us, 3), "gbs": round(gbs, 1), "frac_of_hbm_peak": round(gbs / peak, 4),
             "bytes_per_call": st["bytes"], "launches_per_call": st["launches"], "steps": steps, "note": note}
         del st
+    st = setup_mxfp4(device)
+    ms, _ = time_graphed(st["calls"], 2000, 20, stream, world, device, per_graph=200)
+    us = ms * 1e3 / 2000
+    gbs = st["bytes"] / (us * 1e-6) / 1e9
+    out["mxfp4_experts_6of64_2048x4096"] = {
+        "us_per_call": round(us, 3), "gbs": round(gbs, 1), "frac_of_hbm_peak": round(gbs / peak, 4),
+        "bytes_per_call": st["bytes"], "launches_per_call": 1, "steps": 2000,
+        "note": "the MTP block's OCP MXFP4 experts: one launch, e8m0 per 32 columns decoded in registers"}
     return out
 
 
@@ -559,7 +590,9 @@ def run_profile_workload(args):
     device = torch.device("cuda", 0)
     torch.cuda.set_device(device)
     ops.set_tensor_core_min_m(args.tensor_core_min_m, args.tensor_core_min_bytes)
-    if args.profile_workload.startswith("nvfp4_experts_6of64_2048x4096"):
+    if args.profile_workload == "mxfp4_experts_6of64_2048x4096":
+        st = setup_mxfp4(device)
+    elif args.profile_workload.startswith("nvfp4_experts_6of64_2048x4096"):
         st = setup_nvfp4(device, fused=not args.profile_workload.endswith("_two_step"))
     else:
         st = setup_fp8blk(args.profile_workload, device, args.profile_workload.startswith("head_argmax"))

@@ -8,7 +8,8 @@ raises if it has not been built.  ``synth`` (seeded inputs) imports without it.
 """
 _BINDING_NAMES = (
     "fp8blk_gemv", "fp8blk_gemv_argmax", "fp8blk_gemv_argmax_ws_bytes", "fp8blk_bf16_gemv",
-    "nvfp4_expert_dequant", "nvfp4_expert_dequant_gemv", "nvfp4_expert_gemv", "fp8blk_scales_from_e8m0",
+    "nvfp4_expert_dequant", "nvfp4_expert_dequant_gemv", "nvfp4_expert_gemv", "mxfp4_expert_gemv",
+    "fp8blk_scales_from_e8m0",
     "fp8blk_device_status", "Fp8BlkError", "library_path", "argmax_workspace",
     "set_launch_tuning", "abi_version",
 )

@@ -508,7 +508,30 @@ int nvfp4_expert_gemv(const uint8_t *codes, const uint8_t *scales, const float *
     a.n_active = n_active;
     a.rows = rows;
     a.cols = cols;
-    return from_cuda(launch_nvfp4_gemv(a, dev, static_cast<cudaStream_t>(stream)));
+    return from_cuda(launch_fp4_expert_gemv(a, false, dev, static_cast<cudaStream_t>(stream)));
+}
+
+int mxfp4_expert_gemv(const uint8_t *codes, const uint8_t *scales, int n_experts, const int32_t *ids,
+                      int n_active, const float *x, float *y, int64_t rows, int64_t cols, void *stream) {
+    if (!codes || !scales || !ids || !x || !y || n_experts < 1) return FP8BLK_EINVAL;
+    if (n_active < 1 || n_active > 65536 || rows < 1 || cols < 512 || cols % 512 != 0) return FP8BLK_EINVAL;
+    if (rows > kMaxIndex || cols > kMaxIndex) return FP8BLK_ERANGE;
+    if (!aligned(codes, 16) || !aligned(scales, 16) || !aligned(ids, 4) || !aligned(x, 16) || !aligned(y, 4))
+        return FP8BLK_EALIGN;
+    DeviceInfo dev;
+    if (current_device_info(&dev) != cudaSuccess) return from_cuda(cudaErrorUnknown);
+    Nvfp4Args a = {};
+    a.codes = codes;
+    a.scales = scales;
+    a.ids = ids;
+    a.x = x;
+    a.y = y;
+    a.status = dev.status;
+    a.n_experts = n_experts;
+    a.n_active = n_active;
+    a.rows = rows;
+    a.cols = cols;
+    return from_cuda(launch_fp4_expert_gemv(a, true, dev, static_cast<cudaStream_t>(stream)));
 }
 
 int fp8blk_set_launch_tuning(int target_stage_bytes, int ctas_per_sm, int use_pdl, int l2_prefetch,

@@ -89,8 +89,8 @@ cudaError_t kernel_occupancy(const void *kernel, int threads, size_t smem, int *
 // nvfp4_gemv.cu, which plans the panels, stages and grid itself).
 struct Nvfp4Args {
     const uint8_t *codes;    // [n_experts, rows, cols / 2]
-    const uint8_t *scales;   // [n_experts, rows, cols / 16] e4m3
-    const float *gscale;     // [n_experts], device
+    const uint8_t *scales;   // NVFP4: e4m3 [n_experts, rows, cols / 16]; MXFP4: e8m0 [.., cols / 32]
+    const float *gscale;     // [n_experts], device (NVFP4 only)
     const int32_t *ids;      // [n_active], device
     const float *x;          // [cols]
     float *y;                // [n_active, rows]
@@ -99,11 +99,11 @@ struct Nvfp4Args {
     int64_t rows, cols;
     int panels, panel_cols;  // panel_cols = cols (one panel) or 4096
     int stage_rows;          // R rows per stage
-    int stage_bytes;         // R * (panel_cols / 2 + panel_cols / 16)
+    int stage_bytes;         // R * (panel_cols / 2 + panel_cols / scale_cols)
     int stages;
     int64_t groups;          // row groups per expert: ceil(rows / R)
 };
-cudaError_t launch_nvfp4_gemv(Nvfp4Args a, const DeviceInfo &dev, cudaStream_t stream);
+cudaError_t launch_fp4_expert_gemv(Nvfp4Args a, bool mxfp4, const DeviceInfo &dev, cudaStream_t stream);
 
 // Dynamic shared memory of a planned launch.
 inline size_t plan_smem_bytes(const Plan &p) {

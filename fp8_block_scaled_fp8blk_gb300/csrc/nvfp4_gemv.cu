@@ -1,5 +1,5 @@
-// nvfp4_gemv.cu -- plan and launch of the one-launch NVFP4 routed-expert GEMV
-// (nvfp4_gemv.cuh).
+// nvfp4_gemv.cu -- plan and launch of the one-launch FP4 (NVFP4 / MXFP4)
+// routed-expert GEMV (nvfp4_gemv.cuh).
 #include "launch.h"
 #include "nvfp4_gemv.cuh"
 
@@ -12,10 +12,10 @@
 
 namespace fp8blk {
 
-cudaError_t launch_nvfp4_gemv(Nvfp4Args a, const DeviceInfo &dev, cudaStream_t stream) {
+cudaError_t launch_fp4_expert_gemv(Nvfp4Args a, bool mxfp4, const DeviceInfo &dev, cudaStream_t stream) {
     a.panels = static_cast<int>((a.cols + kNvMaxPanel - 1) / kNvMaxPanel);
     a.panel_cols = a.panels == 1 ? static_cast<int>(a.cols) : kNvMaxPanel;
-    const int row_bytes = a.panel_cols / 2 + a.panel_cols / 16;
+    const int row_bytes = a.panel_cols / 2 + a.panel_cols / (mxfp4 ? 32 : 16);
     // Stages of about 8 KiB (R rows), fewer rows while there are fewer row
     // groups than warps; as many stages as two CTAs per SM leave room for.
     const int ctas_per_sm = 2;
@@ -37,7 +37,9 @@ cudaError_t launch_nvfp4_gemv(Nvfp4Args a, const DeviceInfo &dev, cudaStream_t s
     a.stages = stages;
     const size_t smem = static_cast<size_t>(x_bytes) + static_cast<size_t>(kNvWarps) * stages * a.stage_bytes;
     int per_sm = 0;
-    cudaError_t err = kernel_occupancy(reinterpret_cast<const void *>(nvfp4_gemv_kernel), kNvThreads, smem, &per_sm);
+    const void *kernel = mxfp4 ? reinterpret_cast<const void *>(fp4_expert_gemv_kernel<kFp4Mx>)
+                               : reinterpret_cast<const void *>(fp4_expert_gemv_kernel<kFp4Nv>);
+    cudaError_t err = kernel_occupancy(kernel, kNvThreads, smem, &per_sm);
     if (err != cudaSuccess) return err;
     if (per_sm < 1) return cudaErrorInvalidConfiguration;
     const int64_t total_groups = a.groups * a.n_active;
@@ -56,7 +58,8 @@ cudaError_t launch_nvfp4_gemv(Nvfp4Args a, const DeviceInfo &dev, cudaStream_t s
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = tuning().use_pdl ? 1 : 0;
-    return cudaLaunchKernelEx(&cfg, nvfp4_gemv_kernel, a);
+    return mxfp4 ? cudaLaunchKernelEx(&cfg, fp4_expert_gemv_kernel<kFp4Mx>, a)
+                 : cudaLaunchKernelEx(&cfg, fp4_expert_gemv_kernel<kFp4Nv>, a);
 }
 
 }  // namespace fp8blk

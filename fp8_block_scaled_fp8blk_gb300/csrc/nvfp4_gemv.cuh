@@ -20,6 +20,10 @@
 // An expert id outside [0, n_experts) or a global scale that is not a power
 // of two in [2^-100, 2^100] sets FP8BLK_STATUS_BAD_EXPERT and makes that
 // slot's outputs NaN.
+//
+// The same kernel serves OCP MXFP4 experts (the MTP block's, "Module
+// dsv4_gpu" page, enum ExpertKind): the same code layout, one e8m0 scale
+// 2^(c-127) per 32 columns (0xFF = NaN), no global scale.
 #pragma once
 
 #include "rowwarp_gemv.cuh"
@@ -30,12 +34,27 @@ constexpr int kNvWarps = 4;
 constexpr int kNvThreads = kNvWarps * 32;
 constexpr int kNvMaxPanel = 4096;           // columns per panel (x for 128 columns per lane)
 constexpr unsigned kStatusBadExpert = 2u;   // FP8BLK_STATUS_BAD_EXPERT
+constexpr int kFp4Nv = 0;                   // NVFP4: e4m3 scale per 16 columns, f32 global scale
+constexpr int kFp4Mx = 1;                   // MXFP4: e8m0 scale per 32 columns
+
+template <int FP4>
+__host__ __device__ constexpr int fp4_scale_cols() { return FP4 == kFp4Mx ? 32 : 16; }
+
+// e8m0 code -> 2^(c - 127) as f32 (c = 0 is the subnormal 2^-127), 0xFF -> NaN.
+__device__ __forceinline__ float e8m0_to_f32(uint32_t c) {
+    return __int_as_float(c == 0u ? 0x00400000 : (c == 255u ? 0x7FC00000 : static_cast<int>(c << 23)));
+}
 constexpr int kNvXSmemBytes = kNvMaxPanel * 4;  // one panel of x, lane-transposed (single-panel shapes)
 
 // Expert of slot k, or -1 when the id or its global scale is unusable.
+template <int FP4>
 __device__ __forceinline__ int nv_expert(const Nvfp4Args &a, int k, float *g) {
     const int e = __ldg(a.ids + k);
     if (e < 0 || e >= a.n_experts) return -1;
+    if (FP4 == kFp4Mx) {
+        *g = 1.f;
+        return e;
+    }
     const float gv = __ldg(a.gscale + e);
     int ex = 0;
     const float f = frexpf(gv, &ex);
@@ -45,6 +64,7 @@ __device__ __forceinline__ int nv_expert(const Nvfp4Args &a, int k, float *g) {
 }
 
 // Lane 0: copy unit u (slot k, row group, panel) into a ring stage.
+template <int FP4>
 __device__ __forceinline__ void nv_issue(const Nvfp4Args &a, int64_t u, int64_t n_my, int64_t g0,
                                          uint32_t dst, uint32_t bar, uint64_t policy) {
     const int panel = static_cast<int>(u / n_my);
@@ -53,18 +73,19 @@ __device__ __forceinline__ void nv_issue(const Nvfp4Args &a, int64_t u, int64_t 
     const int64_t row0 = (gg % a.groups) * a.stage_rows;
     const int nr = static_cast<int>(a.rows - row0 < a.stage_rows ? a.rows - row0 : a.stage_rows);
     float g;
-    const int e = nv_expert(a, k, &g);
+    const int e = nv_expert<FP4>(a, k, &g);
     if (e < 0) {  // nothing to copy: complete the phase so the consumers move on
         mbar_arrive(bar);
         return;
     }
     const int64_t pc64 = a.cols - static_cast<int64_t>(panel) * a.panel_cols;
     const int pc = pc64 < a.panel_cols ? static_cast<int>(pc64) : a.panel_cols;
-    const uint32_t cb = static_cast<uint32_t>(pc / 2), sb = static_cast<uint32_t>(pc / 16);
+    constexpr int SC = fp4_scale_cols<FP4>();
+    const uint32_t cb = static_cast<uint32_t>(pc / 2), sb = static_cast<uint32_t>(pc / SC);
     mbar_arrive_expect_tx(bar, static_cast<uint32_t>(nr) * (cb + sb));
     const int64_t erow = static_cast<int64_t>(e) * a.rows + row0;
     const uint8_t *csrc = a.codes + erow * (a.cols / 2) + static_cast<int64_t>(panel) * (a.panel_cols / 2);
-    const uint8_t *ssrc = a.scales + erow * (a.cols / 16) + static_cast<int64_t>(panel) * (a.panel_cols / 16);
+    const uint8_t *ssrc = a.scales + erow * (a.cols / SC) + static_cast<int64_t>(panel) * (a.panel_cols / SC);
     const uint32_t sdst = dst + static_cast<uint32_t>(a.stage_rows) * static_cast<uint32_t>(a.panel_cols / 2);
     if (a.panels == 1) {  // rows are contiguous: one copy each
         bulk_g2s(dst, csrc, static_cast<uint32_t>(nr) * cb, bar, policy);
@@ -72,7 +93,7 @@ __device__ __forceinline__ void nv_issue(const Nvfp4Args &a, int64_t u, int64_t 
     } else {
         for (int r = 0; r < nr; ++r) {
             bulk_g2s(dst + r * cb, csrc + static_cast<int64_t>(r) * (a.cols / 2), cb, bar, policy);
-            bulk_g2s(sdst + r * sb, ssrc + static_cast<int64_t>(r) * (a.cols / 16), sb, bar, policy);
+            bulk_g2s(sdst + r * sb, ssrc + static_cast<int64_t>(r) * (a.cols / SC), sb, bar, policy);
         }
     }
 }
@@ -136,9 +157,9 @@ __device__ __forceinline__ float nv_block16(uint32_t w0, uint32_t w1, const floa
     return s0 + s1;
 }
 
-// This lane's share of one staged row: sum over its chunks of the two blocks'
-// e4m3(s) * (sum of e2m1 * x).
-template <bool FULL>
+// This lane's share of one staged row: sum over its chunks of the chunk's
+// block scale(s) times the sums of e2m1 * x.
+template <int FP4, bool FULL>
 __device__ __forceinline__ float nv_row(const uint8_t *crow, const uint8_t *srow, int lane, int pc,
                                         const float (&xr)[128]) {
     float acc = 0.f;
@@ -147,16 +168,23 @@ __device__ __forceinline__ float nv_row(const uint8_t *crow, const uint8_t *srow
         const int chunk = j * 32 + lane;
         if (FULL || chunk * 32 < pc) {
             const uint4 q = *reinterpret_cast<const uint4 *>(crow + chunk * 16);
-            const uint32_t sc = *reinterpret_cast<const unsigned short *>(srow + chunk * 2);
-            const float2 s = e4m3x2_to_f32(sc);
-            acc = fmaf(s.x, nv_block16(q.x, q.y, &xr[j * 32]), acc);
-            acc = fmaf(s.y, nv_block16(q.z, q.w, &xr[j * 32 + 16]), acc);
+            if (FP4 == kFp4Mx) {  // one e8m0 scale for the chunk's 32 columns
+                const float s = e8m0_to_f32(srow[chunk]);
+                acc = fmaf(s, nv_block16(q.x, q.y, &xr[j * 32]) + nv_block16(q.z, q.w, &xr[j * 32 + 16]), acc);
+            } else {  // two e4m3 scales, one per 16 columns
+                const uint32_t sc = *reinterpret_cast<const unsigned short *>(srow + chunk * 2);
+                const float2 s = e4m3x2_to_f32(sc);
+                acc = fmaf(s.x, nv_block16(q.x, q.y, &xr[j * 32]), acc);
+                acc = fmaf(s.y, nv_block16(q.z, q.w, &xr[j * 32 + 16]), acc);
+            }
         }
     }
     return acc;
 }
 
-__global__ void __launch_bounds__(kNvThreads, 2) nvfp4_gemv_kernel(const Nvfp4Args a) {
+template <int FP4>
+__global__ void __launch_bounds__(kNvThreads, 2) fp4_expert_gemv_kernel(const Nvfp4Args a) {
+    constexpr int SC = fp4_scale_cols<FP4>();
     extern __shared__ __align__(128) uint8_t smem[];
     __shared__ __align__(8) uint64_t bars[kNvWarps][kMaxStages];
 
@@ -187,7 +215,8 @@ __global__ void __launch_bounds__(kNvThreads, 2) nvfp4_gemv_kernel(const Nvfp4Ar
     const int64_t first = units < stages ? units : stages;
     if (lane == 0)
         for (int64_t u = 0; u < first; ++u)
-            nv_issue(a, u, n_my, g0, smem_addr(ring + u * a.stage_bytes), bar0 + 8 * static_cast<uint32_t>(u), policy);
+            nv_issue<FP4>(a, u, n_my, g0, smem_addr(ring + u * a.stage_bytes), bar0 + 8 * static_cast<uint32_t>(u),
+                          policy);
     int64_t issued_end = first;
 
     float xr[128];
@@ -214,7 +243,7 @@ __global__ void __launch_bounds__(kNvThreads, 2) nvfp4_gemv_kernel(const Nvfp4Ar
             cur_panel = panel;
         }
         float g = 0.f;
-        const int e = nv_expert(a, k, &g);
+        const int e = nv_expert<FP4>(a, k, &g);
         const bool ok = mbar_wait_bounded(bar0 + 8 * s, static_cast<uint32_t>((u / stages) & 1));
         if (!__all_sync(0xFFFFFFFFu, ok)) {
             aborted = true;
@@ -231,11 +260,11 @@ __global__ void __launch_bounds__(kNvThreads, 2) nvfp4_gemv_kernel(const Nvfp4Ar
             float pa = 0.f, pb = 0.f;
             if (e >= 0) {
                 if (full) {
-                    pa = nv_row<true>(st + ra * (pc / 2), sst + ra * (pc / 16), lane, pc, xr);
-                    pb = nv_row<true>(st + rb * (pc / 2), sst + rb * (pc / 16), lane, pc, xr);
+                    pa = nv_row<FP4, true>(st + ra * (pc / 2), sst + ra * (pc / SC), lane, pc, xr);
+                    pb = nv_row<FP4, true>(st + rb * (pc / 2), sst + rb * (pc / SC), lane, pc, xr);
                 } else {
-                    pa = nv_row<false>(st + ra * (pc / 2), sst + ra * (pc / 16), lane, pc, xr);
-                    pb = nv_row<false>(st + rb * (pc / 2), sst + rb * (pc / 16), lane, pc, xr);
+                    pa = nv_row<FP4, false>(st + ra * (pc / 2), sst + ra * (pc / SC), lane, pc, xr);
+                    pb = nv_row<FP4, false>(st + rb * (pc / 2), sst + rb * (pc / SC), lane, pc, xr);
                 }
             }
             const float total = warp_sum_two_rows(pa, pb);  // lanes 0-15: row r, 16-31: row rb2
@@ -251,8 +280,8 @@ __global__ void __launch_bounds__(kNvThreads, 2) nvfp4_gemv_kernel(const Nvfp4Ar
         __syncwarp();  // every lane is done reading stage s
         if (u + stages < units) {
             if (lane == 0)
-                nv_issue(a, u + stages, n_my, g0, smem_addr(ring + static_cast<size_t>(s) * a.stage_bytes), bar0 + 8 * s,
-                         policy);
+                nv_issue<FP4>(a, u + stages, n_my, g0, smem_addr(ring + static_cast<size_t>(s) * a.stage_bytes),
+                              bar0 + 8 * s, policy);
             issued_end = u + stages + 1;
         }
     }

@@ -52,6 +52,8 @@ _lib.nvfp4_expert_dequant_gemv.restype = _INT
 _lib.nvfp4_expert_dequant_gemv.argtypes = [_P, _P, _P, _INT, _P, _INT, _P, _P, _P, _I64, _I64, _P]
 _lib.nvfp4_expert_gemv.restype = _INT
 _lib.nvfp4_expert_gemv.argtypes = [_P, _P, _P, _INT, _P, _INT, _P, _P, _I64, _I64, _P]
+_lib.mxfp4_expert_gemv.restype = _INT
+_lib.mxfp4_expert_gemv.argtypes = [_P, _P, _INT, _P, _INT, _P, _P, _I64, _I64, _P]
 _lib.fp8blk_set_launch_tuning.restype = _INT
 _lib.fp8blk_set_launch_tuning.argtypes = [_INT, _INT, _INT, _INT, _INT]
 _lib.fp8blk_set_m1_kernel.restype = _INT
@@ -242,6 +244,22 @@ def nvfp4_expert_gemv(codes: torch.Tensor, scales: torch.Tensor, gscale: torch.T
         y = torch.empty((n_active, rows), dtype=torch.float32, device=x.device)
     _check(_lib.nvfp4_expert_gemv(_ptr(codes), _ptr(scales), _ptr(gscale), n_experts, _ptr(ids), n_active,
                                   _ptr(x), _ptr(y), rows, cols, _stream(x)), "nvfp4_expert_gemv")
+    return y
+
+
+def mxfp4_expert_gemv(codes: torch.Tensor, scales: torch.Tensor, ids: torch.Tensor, x: torch.Tensor,
+                      y: torch.Tensor | None = None) -> torch.Tensor:
+    """OCP MXFP4 experts: y [n_active, rows] = W(ids[k]) x in one launch
+    (e8m0 scale per 32 columns, decoded in registers; `ids` int32 on the device)."""
+    n_experts, rows, half = codes.shape
+    cols = 2 * half
+    if ids.dtype != torch.int32:
+        raise TypeError("ids must be an int32 device tensor")
+    n_active = ids.numel()
+    if y is None:
+        y = torch.empty((n_active, rows), dtype=torch.float32, device=x.device)
+    _check(_lib.mxfp4_expert_gemv(_ptr(codes), _ptr(scales), n_experts, _ptr(ids), n_active, _ptr(x), _ptr(y),
+                                  rows, cols, _stream(x)), "mxfp4_expert_gemv")
     return y
 
 

@@ -43,7 +43,7 @@ extern "C" {
 /* Bits of the device status word (see fp8blk_device_status). */
 #define FP8BLK_STATUS_WAIT_TIMEOUT 1u /* a kernel gave up waiting for a weight tile (bounded
                                          wait, about one second); its outputs are invalid */
-#define FP8BLK_STATUS_BAD_EXPERT 2u   /* nvfp4_expert_gemv met a device-side expert id outside
+#define FP8BLK_STATUS_BAD_EXPERT 2u   /* an expert GEMV met a device-side expert id outside
                                          [0, n_experts) or a global scale that is not a power
                                          of two in [2^-100, 2^100]; that slot's outputs are NaN */
 
@@ -226,6 +226,24 @@ int nvfp4_expert_dequant_gemv(const uint8_t *codes, const uint8_t *scales,
 int nvfp4_expert_gemv(const uint8_t *codes, const uint8_t *scales, const float *gscale, int n_experts,
                       const int32_t *ids, int n_active, const float *x, float *y, int64_t rows, int64_t cols,
                       void *stream);
+
+/*
+ * mxfp4_expert_gemv -- as nvfp4_expert_gemv, for OCP MXFP4 experts (the MTP
+ * block's routed experts, "Module dsv4_gpu" page, enum ExpertKind):
+ *   y[k][r] = sum_c e2m1(q[e][r][c]) * 2^(s[e][r][c/32] - 127) * x[c], e = ids[k].
+ * The page names the format only; the layout is read from the OCP MX format:
+ *   codes        device, uint8 [n_experts, rows, cols/2], two e2m1 codes per
+ *                byte, column 2j in the LOW nibble; 16-byte aligned
+ *   scales       device, uint8 e8m0 [n_experts, rows, cols/32], 16-byte
+ *                aligned; code 0xFF is the MX NaN (its block's weights are NaN)
+ *   ids          DEVICE, int32 [n_active]; repeats allowed
+ *   cols         a multiple of 512 (so every scale row starts on 16 bytes).
+ * No global scale.  An id outside [0, n_experts) sets
+ * FP8BLK_STATUS_BAD_EXPERT and makes y[k] NaN.
+ * Errors: EINVAL, EALIGN, ERANGE, ECUDA.
+ */
+int mxfp4_expert_gemv(const uint8_t *codes, const uint8_t *scales, int n_experts, const int32_t *ids,
+                      int n_active, const float *x, float *y, int64_t rows, int64_t cols, void *stream);
 
 /*
  * fp8blk_set_launch_tuning -- process-wide launch-shape knobs for the

@@ -31,7 +31,8 @@ def declared_functions():
 def test_header_declares_the_boundary_calls():
     names = set(declared_functions())
     for n in ("fp8blk_gemv", "fp8blk_gemv_argmax", "fp8blk_gemv_argmax_ws_bytes",
-              "nvfp4_expert_dequant_gemv", "nvfp4_expert_dequant", "nvfp4_expert_gemv", "fp8blk_scales_from_e8m0",
+              "nvfp4_expert_dequant_gemv", "nvfp4_expert_dequant", "nvfp4_expert_gemv", "mxfp4_expert_gemv",
+              "fp8blk_scales_from_e8m0",
               "fp8blk_strerror", "fp8blk_bf16_gemv", "fp8blk_device_status"):
         assert n in names, n
 
@@ -154,6 +155,23 @@ def test_nvfp4_fused_host_validation(ops):
     assert call(g=None) == ops.EINVAL
     assert call(scales=A4) == ops.EALIGN     # scale rows are bulk-copied: 16-byte aligned
     assert call(codes=A4) == ops.EALIGN
+    assert call(x=A4) == ops.EALIGN
+    assert call(ids=A1) == ops.EALIGN
+    assert call(rows=1 << 40) == ops.ERANGE
+
+
+def test_mxfp4_host_validation(ops):
+    lib = ops.raw_library()
+
+    def call(codes=A16, scales=A16, n=4, ids=A4, k=2, x=A16, y=A4, rows=16, cols=1024):
+        return lib.mxfp4_expert_gemv(codes, scales, n, ids, k, x, y, rows, cols, None)
+
+    assert call(cols=768) == ops.EINVAL      # not a multiple of 512
+    assert call(cols=256) == ops.EINVAL
+    assert call(k=0) == ops.EINVAL
+    assert call(n=0) == ops.EINVAL
+    assert call(ids=None) == ops.EINVAL
+    assert call(scales=A4) == ops.EALIGN
     assert call(x=A4) == ops.EALIGN
     assert call(ids=A1) == ops.EALIGN
     assert call(rows=1 << 40) == ops.ERANGE

@@ -1,0 +1,82 @@
+"""GPU parity of the one-launch OCP MXFP4 routed-expert GEMV (the MTP block's
+experts) against the CPU oracle, through the C ABI.
+
+Bar: outputs within |gpu - oracle| <= 1e-5 * sum|w x| + 1e-6; one-hot x
+reproduces every decoded weight exactly (e2m1 code x e8m0 scale); a 0xFF
+scale poisons only its row; an out-of-range device id gives NaN and the
+status bit.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from _helpers import assert_close, to_dev
+from fp8_block_scaled_fp8blk_gb300 import synth
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def ops():
+    from fp8_block_scaled_fp8blk_gb300 import ops as o
+    yield o
+    assert o.fp8blk_device_status(clear=True) == 0
+
+
+def run(ops, case, ids=None, x=None):
+    ids = case.ids if ids is None else ids
+    x = case.x if x is None else x
+    y = ops.mxfp4_expert_gemv(to_dev(case.codes), to_dev(case.scales), to_dev(np.asarray(ids, dtype=np.int32)),
+                              to_dev(np.asarray(x, dtype=np.float32)))
+    torch.cuda.synchronize()
+    return y.cpu().numpy()
+
+
+def test_mxfp4_full_config(ops):
+    w = synth.MXFP4_WORKLOAD
+    case = synth.mxfp4_case(w["n_experts"], w["rows"], w["cols"], w["n_active"], w["seed"])
+    y = run(ops, case)
+    ref, a = oracle.mxfp4_expert_gemv(case.codes, case.scales, case.ids, case.x, nthreads=16)
+    assert_close(y, ref, a, "mxfp4 6 of 64 2048x4096")
+
+
+@pytest.mark.parametrize("n_experts,rows,cols,n_active", [(3, 1, 512, 1), (4, 7, 1024, 2), (8, 129, 4096, 3),
+                                                          (5, 1000, 1536, 5), (6, 130, 4608, 4), (4, 65, 8192, 4)])
+def test_mxfp4_ragged(ops, n_experts, rows, cols, n_active):
+    case = synth.mxfp4_case(n_experts, rows, cols, n_active, seed=rows * 17 + cols + n_active)
+    y = run(ops, case)
+    ref, a = oracle.mxfp4_expert_gemv(case.codes, case.scales, case.ids, case.x, nthreads=8)
+    assert_close(y, ref, a, f"mxfp4 {n_experts}x{rows}x{cols} k={n_active}")
+
+
+def test_mxfp4_one_hot_is_exact(ops):
+    """Every e2m1 code under e8m0 scales from 2^-127 to 2^127: x = e_c returns
+    the decoded weight column exactly."""
+    rows, cols = 8, 512
+    case = synth.mxfp4_case(1, rows, cols, 1, seed=3)
+    case.codes[0] = np.arange(rows * cols // 2, dtype=np.uint32).reshape(rows, cols // 2).astype(np.uint8)
+    case.scales[0] = np.array([0, 1, 60, 119, 127, 128, 200, 254], dtype=np.uint8)[:, None]
+    for c in (0, 1, 31, 32, 255, 300, 511):
+        x = np.zeros(cols, dtype=np.float32)
+        x[c] = 1.0
+        y = run(ops, case, ids=[0], x=x)
+        ref, _ = oracle.mxfp4_expert_gemv(case.codes, case.scales, np.array([0], dtype=np.int32), x)
+        with np.errstate(over="ignore"):  # 6 * 2^127 is inf in f32 on both sides
+            want = ref[0].astype(np.float32)
+        assert np.array_equal(y[0], want), c
+
+
+def test_mxfp4_scale_ff_poisons_only_its_row(ops):
+    case = synth.mxfp4_case(3, 40, 1024, 2, seed=9)
+    case.scales[case.ids[1], 17, 5] = 0xFF
+    y = run(ops, case)
+    assert np.isnan(y[1, 17]) and not np.isnan(np.delete(y[1], 17)).any() and not np.isnan(y[0]).any()
+
+
+def test_mxfp4_bad_and_repeated_ids(ops):
+    case = synth.mxfp4_case(4, 100, 512, 3, seed=10)
+    assert ops.fp8blk_device_status(clear=True) == 0
+    y = run(ops, case, ids=[2, 7, 2])
+    assert np.isnan(y[1]).all() and np.array_equal(y[0], y[2])
+    assert ops.fp8blk_device_status(clear=True) == ops.STATUS_BAD_EXPERT
