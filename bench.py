@@ -72,8 +72,9 @@ def nvfp4_bytes(n_active: int, rows: int, cols: int) -> int:
 
 
 # Sources that define the streaming kernels and their launch geometry.
-KERNEL_SOURCES = ("device_common.cuh", "stream_gemv.cuh", "rowwarp_gemv.cuh", "tc_gemv.cuh", "launch.h", "abi.cu",
-                  "gemv_e4m3.cu", "gemv_bf16.cu", "gemv_tc.cu", "nvfp4_dequant.cu")
+KERNEL_SOURCES = ("device_common.cuh", "stream_gemv.cuh", "rowwarp_gemv.cuh", "tc_gemv.cuh", "nvfp4_gemv.cuh",
+                  "launch.h", "abi.cu", "gemv_e4m3.cu", "gemv_bf16.cu", "gemv_tc.cu", "nvfp4_dequant.cu",
+                  "nvfp4_gemv.cu")
 
 
 def source_hash() -> str:
