@@ -349,6 +349,56 @@ def test_nvfp4_expert_composite_matches_manual_composition():
             assert np.array_equal(scratch, b)
 
 
+def _nvfp4_decode_numpy(codes, scales, g, block=16, low_first=True):
+    """Independent NVFP4 decode to bf16 bits: golden OCP e2m1 values, torch's
+    float8_e4m3fn decoder for the scales, torch's float -> bfloat16 rounding,
+    and the layout read for the routed experts ("Module dsv4_gpu" page, enum
+    ExpertKind: trunk = modelopt NVFP4): column 2j in the low nibble, one e4m3
+    scale per 16 consecutive columns of a row, one f32 global scale.  `block`
+    and `low_first` exist only so the teeth below can break the layout."""
+    e2m1 = _golden_format_values()["e2m1"]
+    t = np.array([e2m1[n] for n in range(16)], dtype=np.float64)
+    e4 = torch_e4m3_table()
+    lo, hi = codes & 15, codes >> 4
+    nib = np.stack([lo, hi] if low_first else [hi, lo], axis=-1).reshape(codes.shape[:-1] + (2 * codes.shape[-1],))
+    s = np.repeat(e4[scales], block, axis=-1)[..., : nib.shape[-1]]
+    v = torch.from_numpy(t[nib] * s * float(g))
+    return v.float().to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16), v.numpy()
+
+
+@pytest.mark.parametrize("rows,cols,seed", [(37, 256, 21), (5, 4096, 22), (64, 96, 23)])
+def test_nvfp4_matches_independent_decode_and_layout_teeth(rows, cols, seed):
+    """The oracle's bf16 bytes equal an independent decode at widths with many
+    16-column scale blocks per row; a 32-column scale index or a high-nibble-
+    first reading gives different bytes, so either slip fails here."""
+    case = synth.nvfp4_case(n_experts=2, rows=rows, cols=cols, n_active=1, seed=seed)
+    for e in range(2):
+        g = float(case.gscale[e])
+        out, n_inexact = oracle.nvfp4_dequant_bf16(case.codes[e], case.scales[e], g)
+        assert n_inexact == 0
+        want, exact = _nvfp4_decode_numpy(case.codes[e], case.scales[e], g)
+        assert np.array_equal(out, want)
+        # the bf16 bytes carry the exact products (no rounding anywhere)
+        back = torch.from_numpy(want.view(np.int16).copy()).view(torch.bfloat16).double().numpy()
+        assert np.array_equal(back, exact)
+        sc = case.scales[e]
+        by32 = sc[:, np.minimum(np.arange(cols) // 32, sc.shape[1] - 1)]
+        wrong_scale, _ = _nvfp4_decode_numpy(case.codes[e], by32, g, block=1)
+        wrong_nibble, _ = _nvfp4_decode_numpy(case.codes[e], sc, g, low_first=False)
+        assert not np.array_equal(out, wrong_scale)
+        assert not np.array_equal(out, wrong_nibble)
+
+
+def test_nvfp4_expert_gemv_matches_independent_decode_and_matmul():
+    case = synth.nvfp4_case(n_experts=6, rows=33, cols=512, n_active=4, seed=24)
+    y, a, _ = oracle.nvfp4_expert_dequant_gemv(case.codes, case.scales, case.gscale, case.ids, case.x)
+    x = case.x.astype(np.float64)
+    for k, e in enumerate(case.ids):
+        _, w = _nvfp4_decode_numpy(case.codes[e], case.scales[e], float(case.gscale[e]))
+        np.testing.assert_allclose(a[k], np.abs(w) @ np.abs(x), rtol=1e-12)
+        assert np.all(np.abs(y[k] - w @ x) <= 1e-12 * a[k])
+
+
 def test_nvfp4_expert_rejects_bad_ids():
     case = synth.nvfp4_case(n_experts=4, rows=8, cols=32, n_active=2, seed=1)
     for ids in ([0, 0], [0, 4], [-1, 1]):
