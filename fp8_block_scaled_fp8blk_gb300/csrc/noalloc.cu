@@ -61,13 +61,11 @@ extern "C" int fp8blk_gemv_argmax_noalloc(const uint8_t *w_codes, const float *s
     if (!w_codes || !scales || !x || !tokens) return FP8BLK_EINVAL;
     if (m < 1 || m > FP8BLK_MAX_M || rows < 1 || cols < 16 || cols % 16 != 0) return FP8BLK_EINVAL;
     if (rows > (int64_t(1) << 31) - 1 || cols > (int64_t(1) << 31) - 1) return FP8BLK_ERANGE;
-    // The workspace fp8blk_gemv_argmax asks for: counter and per-CTA partials,
-    // plus a panel accumulator when rows are wider than one 4096-column panel.
-    // Shapes that need more than the fixed array are refused.
-    const size_t part_bytes = static_cast<size_t>(fp8blk::kMaxGrid) * m * sizeof(float);
-    size_t need = kCounterBytes + 2 * part_bytes;
-    if (cols > fp8blk::kMaxPanelCols) need += static_cast<size_t>(m) * static_cast<size_t>(rows) * sizeof(float);
-    need = (need + 15) / 16 * 16;
+    // The workspace fp8blk_gemv_argmax asks for this shape (counter, per-CTA
+    // partials, and a panel accumulator when rows are wider than one panel);
+    // shapes that need more than the fixed array are refused.
+    const size_t need = fp8blk_gemv_argmax_ws_bytes(m, rows, cols);
+    if (need == 0) return FP8BLK_EINVAL;
     if (need > kNoAllocScratchBytes) return FP8BLK_ERANGE;
     unsigned char *scratch = nullptr;
     if (scratch_address(&scratch) != cudaSuccess) {
@@ -81,8 +79,7 @@ extern "C" int fp8blk_gemv_argmax_noalloc(const uint8_t *w_codes, const float *s
         (void)cudaGetLastError();
         return FP8BLK_ECUDA;
     }
-    // Hand the scratch to the existing entry point as its workspace.  Its
-    // layout (counter, partial values, partial indices, accumulator) fits in
-    // `need` bytes, which is at most the array's size.
+    // Hand the scratch to the existing entry point as its workspace: `need`
+    // is that entry point's own answer for this shape, at most the array.
     return fp8blk_gemv_argmax(w_codes, scales, x, logits, tokens, scratch, need, m, rows, cols, stream);
 }
