@@ -146,12 +146,24 @@ __global__ void __launch_bounds__(kRowThreads, 2) rowwarp_gemv_kernel(const Gemv
 
     const uint64_t policy = l2_policy_evict_first();
     const int64_t first = units < stages ? units : stages;
-    if (lane == 0 && a.l2_prefetch) {
-        for (int64_t u = 0; u < first; ++u) issue_unit<FMT>(a, u, n_my, g0, 0, 0, policy, true);
+    // e4m3 weight copies of the first stages start before the grid dependency
+    // wait (e4m3 weights are never outputs of the preceding kernel); bf16
+    // weights may be (the NVFP4 expert scratch), so those wait, with only a
+    // coherent L2 prefetch before.  x, the scales and y are only touched after.
+    constexpr bool kEarlyWeights = FMT == kE4M3;
+    if (lane == 0) {
+        const int64_t pf0 = kEarlyWeights ? first : 0;
+        const int64_t pf_end = kEarlyWeights ? (units < 2 * first ? units : 2 * first) : first;
+        if (kEarlyWeights)
+            for (int64_t u = 0; u < first; ++u)
+                issue_unit<FMT>(a, u, n_my, g0, smem_addr(ring + u * a.stage_bytes),
+                                bar0 + 8 * static_cast<uint32_t>(u), policy, false);
+        if (a.l2_prefetch)
+            for (int64_t u = pf0; u < pf_end; ++u) issue_unit<FMT>(a, u, n_my, g0, 0, 0, policy, true);
     }
     grid_dependency_wait();
     grid_launch_dependents();
-    if (lane == 0) {
+    if (!kEarlyWeights && lane == 0) {
         for (int64_t u = 0; u < first; ++u)
             issue_unit<FMT>(a, u, n_my, g0, smem_addr(ring + u * a.stage_bytes), bar0 + 8 * static_cast<uint32_t>(u),
                             policy, false);
@@ -181,7 +193,7 @@ __global__ void __launch_bounds__(kRowThreads, 2) rowwarp_gemv_kernel(const Gemv
             cur_panel = panel;
             cur_rblk = rblk;
         }
-        const bool ok = mbar_wait_bounded(bar0 + 8 * s, static_cast<uint32_t>((u / stages) & 1));
+        const bool ok = mbar_wait_limit(bar0 + 8 * s, static_cast<uint32_t>((u / stages) & 1), a.wait_limit_ns);
         if (!__all_sync(0xFFFFFFFFu, ok)) {
             aborted = true;
             failed_unit = u;

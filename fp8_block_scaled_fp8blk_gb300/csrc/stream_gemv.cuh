@@ -62,6 +62,7 @@ struct GemvArgs {
     int stage_bytes;        // bytes per stage
     int stage_rows;         // R = teams * rb * RT
     int l2_prefetch;        // issue L2 prefetches before the grid-dependency wait
+    uint64_t wait_limit_ns; // consumer-side weight-tile wait limit (drains keep kWaitLimitNs)
 };
 
 __host__ __device__ constexpr int pow2_ceil(int v) {
@@ -370,14 +371,28 @@ __global__ void __launch_bounds__(kThreads, (M <= 4 ? 2 : 1)) stream_gemv_kernel
 
     const uint64_t policy = l2_policy_evict_first();
     const int64_t first = units < stages ? units : stages;
-    if (tid == 0 && a.l2_prefetch) {
-        for (int64_t u = 0; u < first; ++u) issue_unit<FMT>(a, u, n_my, g0, 0, 0, policy, true);
+    // e4m3 weights are never outputs of the preceding kernel on the stream (a
+    // documented contract of the e4m3 entry points), so the first stages'
+    // weight copies start before the grid dependency wait: with programmatic
+    // dependent launch they overlap the tail of the previous call.  bf16
+    // weights can be the preceding dequant kernel's output (the NVFP4 expert
+    // scratch), so they are only prefetched into L2 (coherent) before it.
+    constexpr bool kEarlyWeights = FMT == kE4M3;
+    if (tid == 0) {
+        const int64_t pf0 = kEarlyWeights ? first : 0;
+        const int64_t pf_end = kEarlyWeights ? (units < 2 * first ? units : 2 * first) : first;
+        if (kEarlyWeights)
+            for (int64_t u = 0; u < first; ++u)
+                issue_unit<FMT>(a, u, n_my, g0, smem_addr(stage_base + u * a.stage_bytes),
+                                smem_addr(&full[u]), policy, false);
+        if (a.l2_prefetch)
+            for (int64_t u = pf0; u < pf_end; ++u) issue_unit<FMT>(a, u, n_my, g0, 0, 0, policy, true);
     }
-    // Everything below may read what the previous grid wrote, or overwrite
-    // what it reads.
+    // Everything below may read what the previous grid wrote (x, scales, bf16
+    // weights), or overwrite what it reads (y).
     grid_dependency_wait();
     grid_launch_dependents();
-    if (tid == 0) {
+    if (!kEarlyWeights && tid == 0) {
         for (int64_t u = 0; u < first; ++u)
             issue_unit<FMT>(a, u, n_my, g0, smem_addr(stage_base + u * a.stage_bytes),
                             smem_addr(&full[u]), policy, false);
@@ -405,7 +420,9 @@ __global__ void __launch_bounds__(kThreads, (M <= 4 ? 2 : 1)) stream_gemv_kernel
             cur_panel = panel;
             cur_rblk = rblk;
         }
-        const bool ok = mbar_wait_bounded(smem_addr(&full[s]), static_cast<uint32_t>((u / stages) & 1));
+        // Warp-uniform: the compute below holds warp-wide shuffles.
+        const bool ok = __all_sync(0xFFFFFFFFu, mbar_wait_limit(smem_addr(&full[s]), static_cast<uint32_t>((u / stages) & 1),
+                                                                a.wait_limit_ns));
         if (ok) {
             const uint8_t *st = stage_base + static_cast<size_t>(s) * a.stage_bytes;
             if (pwb == kMaxPanelCols * BPW)
@@ -418,9 +435,8 @@ __global__ void __launch_bounds__(kThreads, (M <= 4 ? 2 : 1)) stream_gemv_kernel
         // The last warp to finish reading stage s refills it, unless some
         // warp's wait timed out (its copy may still be landing in stage s):
         // a failed warp adds 1 to the high half of the arrival word.
-        const bool warp_ok = __all_sync(0xFFFFFFFFu, ok);
         if (lane == 0) {
-            const unsigned int inc = warp_ok ? 1u : 0x10001u;
+            const unsigned int inc = ok ? 1u : 0x10001u;
             const unsigned int total = atomicAdd(&consumed[s], inc) + inc;
             if ((total & 0xFFFFu) == kWarps) {
                 consumed[s] = 0;
@@ -468,10 +484,11 @@ __global__ void __launch_bounds__(kThreads, (M <= 4 ? 2 : 1)) stream_gemv_kernel
     }
 
     if (aborted) {
-        // Units up to failed_unit + stages - 1 (and possibly the next) have
-        // been issued; let those copies land before the shared memory is
-        // released (each wait bounded), then report.
-        const int64_t issued_end = failed_unit + stages + 1 < units ? failed_unit + stages + 1 : units;
+        // Units up to failed_unit + stages - 1 have been issued (a failed warp
+        // stops the refill of failed_unit + stages); let those copies land
+        // before the shared memory is released (each wait bounded by the fixed
+        // limit), then report.
+        const int64_t issued_end = failed_unit + stages < units ? failed_unit + stages : units;
         for (int64_t u = failed_unit; u < issued_end; ++u)
             (void)mbar_wait_bounded(smem_addr(&full[u % stages]), static_cast<uint32_t>((u / stages) & 1));
         if (tid == 0) atomicOr(a.status, 1u);

@@ -13,6 +13,21 @@
  *     error nothing is launched and the return value says why.
  *   - Matrices are row-major and dense (row stride = number of columns).
  *   - Integer sizes are int64_t; the product rows * cols may exceed 2^31.
+ *   - Launch contract for e4m3 weight codes (fp8blk_gemv, fp8blk_gemv_argmax,
+ *     fp8blk_gemv_argmax_noalloc): kernels are launched with programmatic
+ *     dependent launch and start copying the weight codes as soon as they are
+ *     resident, which can be before the kernel launched just before them on
+ *     the same stream has finished; x, scales and outputs are touched only
+ *     after that kernel has completed.  So the codes must not be written by
+ *     that immediately preceding kernel (nor by a kernel it lets run
+ *     concurrently by triggering its dependents before waiting on its own
+ *     predecessors; the library's kernels never do).  Codes written by a copy,
+ *     a memset, or any earlier kernel are safe -- weights loaded once at start
+ *     up, as the pages' engine keeps them ("Module dsv4_gpu" page, struct
+ *     Fp8Dense), always are.  fp8blk_set_launch_tuning(.., use_pdl = 0, ..)
+ *     turns the early start off.  bf16 and FP4 weights are read only after
+ *     the preceding kernel has completed (the bf16 GEMV's weights can be the
+ *     dequant kernel's output).
  *
  * Return codes (int): FP8BLK_OK on success, otherwise one of the codes below;
  * fp8blk_strerror() names them.
@@ -253,14 +268,33 @@ int mxfp4_expert_gemv(const uint8_t *codes, const uint8_t *scales, int n_experts
  *   target_stage_bytes  weight bytes per shared-memory pipeline stage (32 KiB)
  *   ctas_per_sm         resident CTAs per SM, 1..4 (2 for m <= 4, else 1)
  *   use_pdl             programmatic dependent launch on (nonzero) or off
- *   l2_prefetch         L2 prefetch of the first stages before the grid
- *                       dependency wait, on (nonzero) or off
+ *   l2_prefetch         L2 prefetch, before the grid dependency wait, of the
+ *                       stages after the first ring (e4m3) or of the first
+ *                       stages (bf16), on (nonzero) or off
  *   max_stages          pipeline depth cap, 2..8 (8)
  * Not thread-safe against concurrent calls of the other entry points.
  * Errors: EINVAL.
  */
 int fp8blk_set_launch_tuning(int target_stage_bytes, int ctas_per_sm, int use_pdl, int l2_prefetch,
                              int max_stages);
+
+/*
+ * fp8blk_set_wait_limit -- process-wide limit (nanoseconds, 0 ..
+ * FP8BLK_WAIT_LIMIT_DEFAULT_NS) on how long a kernel thread of the CUDA-core
+ * GEMVs (fp8blk_gemv / fp8blk_gemv_argmax below the tensor-core thresholds,
+ * fp8blk_bf16_gemv, nvfp4_expert_gemv, mxfp4_expert_gemv) waits for a weight
+ * tile before it gives up, sets FP8BLK_STATUS_WAIT_TIMEOUT and returns.  The
+ * default is about one second; a healthy tile lands in microseconds, so any
+ * shorter limit is for exercising the failure path (0 gives up on the first
+ * tile that has not landed yet).  After a give-up the CTA still waits, with
+ * the fixed one-second bound, for the copies it has in flight before it
+ * exits, and still takes part in the argmax hand-off, so the workspace stays
+ * consistent; the outputs of that call are invalid.  The tensor-core kernel
+ * and the dequant kernel keep the fixed bound.  Not thread-safe against
+ * concurrent calls of the other entry points.  Errors: EINVAL.
+ */
+#define FP8BLK_WAIT_LIMIT_DEFAULT_NS 1000000000ll
+int fp8blk_set_wait_limit(int64_t limit_ns);
 
 /*
  * fp8blk_set_m1_kernel -- which kernel serves m = 1 (speed only; results are
