@@ -262,6 +262,7 @@ void apply_plan(const Plan &p, GemvArgs *a) {
     a->stage_bytes = p.stage_bytes;
     a->stage_rows = p.stage_rows;
     a->l2_prefetch = tuning().l2_prefetch;
+    a->wait_limit_ns = tuning().wait_limit_ns;
 }
 
 }  // namespace fp8blk
@@ -508,6 +509,7 @@ int nvfp4_expert_gemv(const uint8_t *codes, const uint8_t *scales, const float *
     a.n_active = n_active;
     a.rows = rows;
     a.cols = cols;
+    a.wait_limit_ns = tuning().wait_limit_ns;
     return from_cuda(launch_fp4_expert_gemv(a, false, dev, static_cast<cudaStream_t>(stream)));
 }
 
@@ -531,6 +533,7 @@ int mxfp4_expert_gemv(const uint8_t *codes, const uint8_t *scales, int n_experts
     a.n_active = n_active;
     a.rows = rows;
     a.cols = cols;
+    a.wait_limit_ns = tuning().wait_limit_ns;
     return from_cuda(launch_fp4_expert_gemv(a, true, dev, static_cast<cudaStream_t>(stream)));
 }
 
@@ -545,6 +548,12 @@ int fp8blk_set_launch_tuning(int target_stage_bytes, int ctas_per_sm, int use_pd
     t.use_pdl = use_pdl != 0;
     t.l2_prefetch = l2_prefetch != 0;
     t.max_stages = max_stages ? max_stages : kMaxStages;
+    return FP8BLK_OK;
+}
+
+int fp8blk_set_wait_limit(int64_t limit_ns) {
+    if (limit_ns < 0 || limit_ns > FP8BLK_WAIT_LIMIT_DEFAULT_NS) return FP8BLK_EINVAL;
+    tuning().wait_limit_ns = static_cast<uint64_t>(limit_ns);
     return FP8BLK_OK;
 }
 

@@ -87,6 +87,34 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity)
     }
 }
 
+// Non-blocking test of phase `parity` (never suspends the thread).
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// A consumer's wait for a weight tile with a process-wide limit (set on the
+// host, fp8blk_set_wait_limit).  At the default limit this is
+// mbar_wait_bounded; a shorter limit polls without sleeping, so a limit of 0
+// gives up unless the phase has already completed.  Drains of copies still in
+// flight never use this: they keep the fixed kWaitLimitNs bound, so a CTA
+// never exits with a copy landing in its shared memory.
+template <bool SLEEP = true>
+__device__ __forceinline__ bool mbar_wait_limit(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
+    if (limit_ns >= kWaitLimitNs) return mbar_wait_bounded<SLEEP>(bar, parity);
+    const uint64_t t0 = global_timer_ns();
+    while (!mbar_test_wait(bar, parity))
+        if (global_timer_ns() - t0 >= limit_ns) return false;
+    return true;
+}
+
 // Plain arrive (release) on a barrier, e.g. "this warp is done with a stage".
 __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
     asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");

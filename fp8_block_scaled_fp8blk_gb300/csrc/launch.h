@@ -24,6 +24,7 @@ struct Tuning {
     int tc_min_m = 5;                    // tensor-core kernel for m >= this (9 = never)
     int64_t tc_min_bytes = 32ll << 20;   // ... and at least this many weight bytes
     int64_t m1_rowwarp_min_bytes = 96ll << 20;  // by size: row-per-warp from this many weight bytes
+    uint64_t wait_limit_ns = kWaitLimitNs;      // consumer waits of the CUDA-core kernels
 };
 Tuning &tuning();
 
@@ -102,6 +103,7 @@ struct Nvfp4Args {
     int stage_bytes;         // R * (panel_cols / 2 + panel_cols / scale_cols)
     int stages;
     int64_t groups;          // row groups per expert: ceil(rows / R)
+    uint64_t wait_limit_ns;  // consumer-side weight-tile wait limit
 };
 cudaError_t launch_fp4_expert_gemv(Nvfp4Args a, bool mxfp4, const DeviceInfo &dev, cudaStream_t stream);
 

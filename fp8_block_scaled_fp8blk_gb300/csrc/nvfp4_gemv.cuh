@@ -244,7 +244,7 @@ __global__ void __launch_bounds__(kNvThreads, 2) fp4_expert_gemv_kernel(const Nv
         }
         float g = 0.f;
         const int e = nv_expert<FP4>(a, k, &g);
-        const bool ok = mbar_wait_bounded(bar0 + 8 * s, static_cast<uint32_t>((u / stages) & 1));
+        const bool ok = mbar_wait_limit(bar0 + 8 * s, static_cast<uint32_t>((u / stages) & 1), a.wait_limit_ns);
         if (!__all_sync(0xFFFFFFFFu, ok)) {
             aborted = true;
             failed_unit = u;

@@ -58,6 +58,8 @@ _lib.fp8blk_set_launch_tuning.restype = _INT
 _lib.fp8blk_set_launch_tuning.argtypes = [_INT, _INT, _INT, _INT, _INT]
 _lib.fp8blk_set_m1_kernel.restype = _INT
 _lib.fp8blk_set_m1_kernel.argtypes = [_INT, _I64]
+_lib.fp8blk_set_wait_limit.restype = _INT
+_lib.fp8blk_set_wait_limit.argtypes = [_I64]
 _lib.fp8blk_set_tensor_core_min_m.restype = _INT
 _lib.fp8blk_set_tensor_core_min_m.argtypes = [_INT, _I64]
 _lib.fp8blk_plan_query.restype = _INT
@@ -293,6 +295,15 @@ def set_tensor_core_min_m(min_m: int = 0, min_bytes: int = 0) -> None:
     """e4m3 GEMVs with m >= min_m (2..8; 9 = never) and at least min_bytes of
     weights (1 = any) run on the tensor cores; 0 restores a default."""
     _check(_lib.fp8blk_set_tensor_core_min_m(min_m, min_bytes), "fp8blk_set_tensor_core_min_m")
+
+
+WAIT_LIMIT_DEFAULT_NS = 1_000_000_000
+
+
+def set_wait_limit(limit_ns: int = WAIT_LIMIT_DEFAULT_NS) -> None:
+    """How long a CUDA-core GEMV thread waits for a weight tile before giving
+    up (status FP8BLK_STATUS_WAIT_TIMEOUT); the default is about one second."""
+    _check(_lib.fp8blk_set_wait_limit(int(limit_ns)), "fp8blk_set_wait_limit")
 
 
 def fp8blk_device_status(clear: bool = False) -> int:

@@ -182,3 +182,8 @@ def test_tuning_validation(ops):
     assert lib.fp8blk_set_launch_tuning(0, 5, 1, 1, 0) == ops.EINVAL
     assert lib.fp8blk_set_launch_tuning(0, 0, 1, 1, 1) == ops.EINVAL
     assert lib.fp8blk_set_launch_tuning(0, 0, 1, 1, 0) == ops.OK
+    lib.fp8blk_set_wait_limit.argtypes = [ctypes.c_int64]
+    assert lib.fp8blk_set_wait_limit(-1) == ops.EINVAL
+    assert lib.fp8blk_set_wait_limit(ops.WAIT_LIMIT_DEFAULT_NS + 1) == ops.EINVAL
+    assert lib.fp8blk_set_wait_limit(0) == ops.OK
+    assert lib.fp8blk_set_wait_limit(ops.WAIT_LIMIT_DEFAULT_NS) == ops.OK
