@@ -1,13 +1,23 @@
 #!/usr/bin/env python3
 """Benchmark of the FP8-blk decode GEMV hot path on GB300.
 
-Headline workload: the FP8-blk dense-linear GEMV, W 4096 x 4096 e4m3 codes with
-a 32 x 32 grid of e8m0 block scales (decoded to f32 on the host), x f32 [1, 4096],
-y f32 [1, 4096].  One step = one fp8blk_gemv call (one kernel launch) on one
-weight matrix with one activation row.  Weights, scales and x are resident in
-HBM before the timed region; the timed region replays CUDA graphs of
-back-to-back calls that rotate over enough distinct weight copies that their
-total exceeds L2 (so every call streams its weights from HBM).
+Headline workload (the largest configuration): the vocab-head GEMV fused with
+the greedy argmax, W 131072 x 4096 e4m3 codes with a 1024 x 32 grid of e8m0
+block scales (decoded to f32 on the host), x f32 [1, 4096]; the call returns
+one u32 token.  One step = one fp8blk_gemv_argmax call (one kernel launch).
+Weights, scales and x are resident in HBM before the timed region; calls
+rotate over enough weight copies that their total exceeds L2, so every call
+streams its weights from HBM.
+
+Timing: W untimed warm-up calls, then CUDA graphs of exactly K back-to-back
+calls (K = --steps), replayed as repetitions -- at least five, and until a
+minimum time has passed -- each bracketed by a barrier and a device
+synchronize and timed with CUDA events on the launch stream.  The reported
+time per step is the median over repetitions (max over ranks); clock samples
+come from inside the repetitions' window.  The other workloads of the path
+(the 4096 x 4096 and 512 x 1024 GEMVs, the m = 8 verify on the tensor-core and
+CUDA-core kernels, the NVFP4 and MXFP4 experts) are timed the same way into
+`workloads`.
 
 Metric: algorithmic bytes (codes + f32 scales + activations + outputs) per
 second, GB/s, and its fraction of the measured HBM peak; microseconds per call.
@@ -38,7 +48,8 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "FP8-blk decode GEMV weight GB/s (fraction of GB300 HBM peak); us per call"
-HEADLINE = "gemv_4096x4096_m1"
+HEADLINE = "head_argmax_131072x4096_m1"
+HEADLINE_ARGMAX = True
 L2_BYTES = 129 * 1024 * 1024
 FALLBACK_HBM_GBS = 6800.0
 CSRC = os.path.join(ROOT, "fp8_block_scaled_fp8blk_gb300", "csrc")
@@ -213,11 +224,14 @@ def barrier(world: int):
 
 
 # ---------------------------------------------------------------- timing core
-def time_graphed(calls, steps: int, warmup: int, stream, world: int, device, sampler=None,
-                 per_graph: int = 1000):
-    """Run `warmup` eager calls, then exactly `steps` calls replayed from CUDA
-    graphs on `stream`; returns (elapsed ms over the steps, max over ranks,
-    host window)."""
+def time_reps(calls, steps: int, warmup: int, stream, world: int, device, min_reps: int = 5,
+              min_seconds: float = 0.3, max_reps: int = 3000, per_graph: int = 1000) -> dict:
+    """`warmup` eager calls, then CUDA graphs of exactly `steps` back-to-back
+    calls on `stream`, replayed as repetitions: at least `min_reps`, and until
+    `min_seconds` of wall time have passed.  Each repetition is bracketed by a
+    barrier and a device synchronize and timed with CUDA events on `stream`.
+    Returns the median / min / max milliseconds per repetition (each the max
+    over ranks), the repetition count and the host window of the repetitions."""
     import torch
     n = len(calls)
     with torch.cuda.stream(stream):
@@ -225,41 +239,42 @@ def time_graphed(calls, steps: int, warmup: int, stream, world: int, device, sam
             calls[i % n]()
     stream.synchronize()
 
-    def capture(count):
+    def capture(first, count):
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=stream):
-            for i in range(count):
+            for i in range(first, first + count):
                 calls[i % n]()
         return g
 
-    per_graph = max(n, (per_graph // n) * n)
-    full, rem = divmod(steps, per_graph)
-    g_full = capture(per_graph) if full else None
-    g_rem = capture(rem) if rem else None
+    graphs, done = [], 0
+    while done < steps:  # one repetition = these graphs in order = exactly `steps` calls
+        k = min(per_graph, steps - done)
+        graphs.append(capture(done, k))
+        done += k
     with torch.cuda.stream(stream):  # warm the graphs themselves (untimed)
-        if g_full is not None:
-            g_full.replay()
-        if g_rem is not None:
-            g_rem.replay()
+        for g in graphs:
+            g.replay()
     stream.synchronize()
     start = torch.cuda.Event(enable_timing=True)
     end = torch.cuda.Event(enable_timing=True)
-    torch.cuda.synchronize()
-    barrier(world)
-    torch.cuda.synchronize()
+    ms = []
     t0 = time.time()
-    with torch.cuda.stream(stream):
-        start.record(stream)
-        for _ in range(full):
-            g_full.replay()
-        if g_rem is not None:
-            g_rem.replay()
-        end.record(stream)
-    torch.cuda.synchronize()
+    while len(ms) < min_reps or (time.time() - t0 < min_seconds and len(ms) < max_reps):
+        torch.cuda.synchronize()
+        barrier(world)
+        torch.cuda.synchronize()
+        with torch.cuda.stream(stream):
+            start.record(stream)
+            for g in graphs:
+                g.replay()
+            end.record(stream)
+        torch.cuda.synchronize()
+        ms.append(start.elapsed_time(end))
     t1 = time.time()
     barrier(world)
-    ms = start.elapsed_time(end)
-    return max_over_ranks(ms, world, device), (t0, t1)
+    med = statistics.median(ms)
+    return {"ms": max_over_ranks(med, world, device), "ms_min": max_over_ranks(min(ms), world, device),
+            "ms_max": max_over_ranks(max(ms), world, device), "reps": len(ms), "window": (t0, t1)}
 
 
 # ---------------------------------------------------------------- workloads
@@ -288,6 +303,7 @@ def setup_fp8blk(name: str, device, argmax: bool = False):
     ws_ = [w0] + [w0.clone() for _ in range(n - 1)]
     x = up(case.x, device)
     calls = []
+    wsp = toks = None
     if argmax:
         wsp = [ops.argmax_workspace(m, rows, cols, device) for _ in range(n)]
         toks = [torch.empty(m, dtype=torch.int32, device=device) for _ in range(n)]
@@ -298,7 +314,7 @@ def setup_fp8blk(name: str, device, argmax: bool = False):
         for i in range(n):
             calls.append(lambda i=i: ops.fp8blk_gemv(ws_[i], s, x, y=ys[i]))
     return dict(case=case, calls=calls, copies=n, rows=rows, cols=cols, m=m, weights=ws_, scales=s,
-                bytes=fp8blk_bytes(rows, cols, m, argmax))
+                x=x, workspaces=wsp, argmax=argmax, launches=1, bytes=fp8blk_bytes(rows, cols, m, argmax))
 
 
 def setup_nvfp4(device, fused: bool = True):
@@ -354,23 +370,42 @@ def setup_mxfp4(device):
     return dict(calls=calls, bytes=mxfp4_bytes(w["n_active"], w["rows"], w["cols"]), launches=1)
 
 
-def measure_extra(device, stream, world, peak):
-    """The other workloads of the path, measured the same way (one JSON line)."""
+def summarize(st: dict, r: dict, steps: int, peak: float, sampler, **extra) -> dict:
+    """One workload's entry: median us per call and its GB/s over the repetitions."""
+    us = r["ms"] * 1e3 / steps
+    gbs = st["bytes"] / (us * 1e-6) / 1e9
+    out = {"us_per_call": round(us, 3), "gbs": round(gbs, 1), "frac_of_hbm_peak": round(gbs / peak, 4),
+           "bytes_per_call": st["bytes"], "steps": steps, "repetitions": r["reps"],
+           "us_per_call_min_max": [round(r["ms_min"] * 1e3 / steps, 3), round(r["ms_max"] * 1e3 / steps, 3)],
+           "launches_per_call": st.get("launches", 1)}
+    if sampler is not None:
+        out["clocks"] = sampler.summary(*r["window"])
+    out.update(extra)
+    return out
+
+
+def measure_extra(device, stream, world, peak, steps, warmup, sampler):
+    """The other workloads of the path, timed the same way (one JSON line)."""
     from fp8_block_scaled_fp8blk_gb300 import ops
     out = {}
-    for name, argmax, steps in (("gemv_512x1024_m1", False, 4000),
-                                ("head_argmax_131072x4096_m1", True, 300),
-                                ("verify_16384x4096_m8", False, 2000)):
-        st = setup_fp8blk(name, device, argmax)
-        ms, _ = time_graphed(st["calls"], steps, 20, stream, world, device,
-                             per_graph=200 if argmax else 1000)
-        us = ms * 1e3 / steps
-        gbs = st["bytes"] / (us * 1e-6) / 1e9
-        out[name] = {"us_per_call": round(us, 3), "gbs": round(gbs, 1),
-                     "frac_of_hbm_peak": round(gbs / peak, 4), "bytes_per_call": st["bytes"],
-                     "weight_copies": st["copies"], "steps": steps,
-                     "kernel": kernel_name(ops, st["m"], st["rows"], st["cols"], argmax)}
+    for name in ("gemv_512x1024_m1", "gemv_4096x4096_m1"):
+        st = setup_fp8blk(name, device)
+        r = time_reps(st["calls"], steps, warmup, stream, world, device)
+        out[name] = summarize(st, r, steps, peak, sampler, weight_copies=st["copies"],
+                              kernel=kernel_name(ops, st["m"], st["rows"], st["cols"]))
         del st
+    # The m = 8 verify on both kernels: the tensor-core kernel (the library's
+    # default for m >= 5 and >= 32 MiB of weights) and the CUDA-core team kernel.
+    name = "verify_16384x4096_m8"
+    st = setup_fp8blk(name, device)
+    for arm, min_m in (("tensor_core", 0), ("cuda_core", 9)):
+        ops.set_tensor_core_min_m(min_m, 0)
+        r = time_reps(st["calls"], steps, warmup, stream, world, device)
+        key = name if arm == "tensor_core" else name + "_cuda_core"
+        out[key] = summarize(st, r, steps, peak, sampler, weight_copies=st["copies"],
+                             kernel=kernel_name(ops, st["m"], st["rows"], st["cols"]))
+    ops.set_tensor_core_min_m(0, 0)
+    del st
     for fused, name, note in (
             (True, "nvfp4_experts_6of64_2048x4096",
              "one launch: NVFP4 decoded in registers, expert ids and global scales on the device"),
@@ -378,77 +413,97 @@ def measure_extra(device, stream, world, peak):
              "dequant to the reused bf16 scratch + bf16 GEMV per expert; algorithmic bytes exclude "
              "the 2 x 16 MiB scratch write+read per expert")):
         st = setup_nvfp4(device, fused)
-        steps = 2000 if fused else 500
-        ms, _ = time_graphed(st["calls"], steps, 20, stream, world, device, per_graph=200 if fused else 100)
-        us = ms * 1e3 / steps
-        gbs = st["bytes"] / (us * 1e-6) / 1e9
-        out[name] = {
-            "us_per_call": round(us, 3), "gbs": round(gbs, 1), "frac_of_hbm_peak": round(gbs / peak, 4),
-            "bytes_per_call": st["bytes"], "launches_per_call": st["launches"], "steps": steps, "note": note}
+        r = time_reps(st["calls"], steps, warmup, stream, world, device)
+        out[name] = summarize(st, r, steps, peak, sampler, note=note)
         del st
     st = setup_mxfp4(device)
-    ms, _ = time_graphed(st["calls"], 2000, 20, stream, world, device, per_graph=200)
-    us = ms * 1e3 / 2000
-    gbs = st["bytes"] / (us * 1e-6) / 1e9
-    out["mxfp4_experts_6of64_2048x4096"] = {
-        "us_per_call": round(us, 3), "gbs": round(gbs, 1), "frac_of_hbm_peak": round(gbs / peak, 4),
-        "bytes_per_call": st["bytes"], "launches_per_call": 1, "steps": 2000,
-        "note": "the MTP block's OCP MXFP4 experts: one launch, e8m0 per 32 columns decoded in registers"}
+    r = time_reps(st["calls"], steps, warmup, stream, world, device)
+    out["mxfp4_experts_6of64_2048x4096"] = summarize(
+        st, r, steps, peak, sampler,
+        note="the MTP block's OCP MXFP4 experts: one launch, e8m0 per 32 columns decoded in registers")
     return out
 
 
-def measure_e2e(st, steps: int, device) -> dict:
+def measure_e2e(st, steps: int, device, min_seconds: float = 0.5) -> dict:
     """Same metric through the public API with host buffers: per step, copy x
-    from pinned host memory, run the GEMV, read y back, synchronize."""
+    from pinned host memory, run the call, read its result (the u32 token for
+    the argmax, y otherwise) back into pinned memory, synchronize."""
     import torch
     from fp8_block_scaled_fp8blk_gb300 import ops
     case = st["case"]
     x_h = torch.from_numpy(case.x.copy()).pin_memory()
-    y_h = torch.empty((st["m"], st["rows"]), dtype=torch.float32).pin_memory()
     x_d = torch.empty_like(x_h, device=device)
-    y_d = torch.empty((st["m"], st["rows"]), dtype=torch.float32, device=device)
     s = st["scales"]
     n = len(st["weights"])
     stream = torch.cuda.current_stream(device)
+    if st["argmax"]:
+        out_d = torch.empty(st["m"], dtype=torch.int32, device=device)
+        wsp = st["workspaces"]
+
+        def run(i):
+            ops.fp8blk_gemv_argmax(st["weights"][i % n], s, x_d, wsp[i % n], tokens=out_d)
+    else:
+        out_d = torch.empty((st["m"], st["rows"]), dtype=torch.float32, device=device)
+
+        def run(i):
+            ops.fp8blk_gemv(st["weights"][i % n], s, x_d, y=out_d)
+    out_h = torch.empty(out_d.shape, dtype=out_d.dtype).pin_memory()
 
     def one(i):
         x_d.copy_(x_h, non_blocking=True)
-        ops.fp8blk_gemv(st["weights"][i % n], s, x_d, y=y_d)
-        y_h.copy_(y_d, non_blocking=True)
+        run(i)
+        out_h.copy_(out_d, non_blocking=True)
         stream.synchronize()
 
-    for i in range(20):
+    for i in range(10):
         one(i)
-    k = max(1, min(steps, 20000))
-    t0 = time.perf_counter()
-    for i in range(k):
-        one(i)
+    k, t0 = 0, time.perf_counter()
+    while k < max(steps, 5) or time.perf_counter() - t0 < min_seconds:
+        one(k)
+        k += 1
     dt = (time.perf_counter() - t0) / k
     return {"value": round(st["bytes"] / dt / 1e9, 2), "unit": "GB/s", "us_per_call": round(dt * 1e6, 3),
-            "steps": k, "h2d_bytes_per_step": x_h.numel() * 4, "d2h_bytes_per_step": y_h.numel() * 4}
+            "steps": k, "h2d_bytes_per_step": x_h.numel() * 4,
+            "d2h_bytes_per_step": out_h.numel() * out_h.element_size(),
+            "path": "Python binding: pinned x -> device, one library call, result -> pinned host, stream sync"}
 
 
-def cpu_baseline(name: str, budget_s: float = 8.0) -> dict:
-    """The oracle, as it stands, on this host's cores: whole GEMV calls of the
-    same workload for about budget_s seconds."""
+def oracle_rate(name: str, argmax: bool, nthreads: int, budget_s: float, rows_per_call: int) -> dict:
+    """The oracle, as it stands, on `nthreads` host threads: calls on the
+    first `rows_per_call` rows of the workload (its argmax too, for the head)
+    for about budget_s seconds; GB/s of the sampled rows' algorithmic bytes."""
     import oracle
     from fp8_block_scaled_fp8blk_gb300 import synth
     w = synth.WORKLOADS[name]
     case = synth.workload_case(name)
-    cores = os.cpu_count() or 1
     oracle.build()
+    r = min(rows_per_call, w["rows"])
+    codes, grid = case.codes[:r], case.scale_e8m0[:math.ceil(r / 128)]
     t0 = time.perf_counter()
     n = 0
     while True:
-        oracle.fp8blk_gemv(case.codes, case.scale_e8m0, case.x, nthreads=cores)
+        y, _ = oracle.fp8blk_gemv(codes, grid, case.x, nthreads=nthreads)
+        if argmax:
+            for i in range(w["m"]):
+                oracle.argmax(y[i])
         n += 1
         el = time.perf_counter() - t0
         if el >= budget_s:
             break
-    nbytes = fp8blk_bytes(w["rows"], w["cols"], w["m"])
-    return {"value": round(nbytes * n / el / 1e9, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
-            "sample": f"{n} whole {w['rows']}x{w['cols']} m={w['m']} calls in {el:.1f} s "
-                      f"(double-precision oracle, {cores} threads)"}
+    nbytes = fp8blk_bytes(r, w["cols"], w["m"], argmax)
+    return {"value": round(nbytes * n / el / 1e9, 4), "unit": "GB/s", "cores": nthreads,
+            "sample": f"{n} calls on rows 0..{r - 1} of {w['rows']}x{w['cols']} m={w['m']}"
+                      f"{' (+argmax)' if argmax else ''} in {el:.1f} s"}
+
+
+def cpu_baseline(name: str, argmax: bool) -> dict:
+    """The oracle timed on one host thread and on every host core."""
+    cores = os.cpu_count() or 1
+    one = oracle_rate(name, argmax, 1, 6.0, 2048)
+    allc = oracle_rate(name, argmax, cores, 6.0, 16384)
+    return {"value": allc["value"], "unit": "GB/s", "cores": cores, "kind": "oracle",
+            "sample": allc["sample"] + f"; double-precision oracle on {cores} threads",
+            "single_thread": {"value": one["value"], "unit": "GB/s", "cores": 1, "sample": one["sample"]}}
 
 
 # ---------------------------------------------------------------- arms
@@ -464,7 +519,7 @@ def run_ours(args):
     ops.set_tensor_core_min_m(args.tensor_core_min_m, args.tensor_core_min_bytes)
     peak, peak_src = hbm_peak()
     stream = torch.cuda.Stream(device)
-    st = setup_fp8blk(HEADLINE, device)
+    st = setup_fp8blk(HEADLINE, device, HEADLINE_ARGMAX)
     try:
         uuid = str(torch.cuda.get_device_properties(device).uuid)
         uuid = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
@@ -472,43 +527,54 @@ def run_ours(args):
         uuid = None
     sampler = ClockSampler(uuid) if rank == 0 else None
     time.sleep(0.3)
-    ms, (t0, t1) = time_graphed(st["calls"], args.steps, args.warmup, stream, world, device)
-    clocks = sampler.summary(t0, t1) if sampler else None
-    if sampler:
-        sampler.stop()
+    r = time_reps(st["calls"], args.steps, args.warmup, stream, world, device, min_seconds=1.0)
+    clocks = sampler.summary(*r["window"]) if sampler else None
+    ms = r["ms"]
     us = ms * 1e3 / args.steps
     per_gpu_gbs = st["bytes"] / (us * 1e-6) / 1e9
     value = replica_throughput(st["bytes"], us, world)
     status = ops.fp8blk_device_status()
     e2e = measure_e2e(st, args.steps, device)
     e2e["value"] = round(e2e["value"] * world, 2) if world > 1 else e2e["value"]
+    del st
     extra = None
     if world == 1 and not args.no_extra:
-        extra = measure_extra(device, stream, world, peak)
+        extra = measure_extra(device, stream, world, peak, args.steps, args.warmup, sampler)
+    if sampler:
+        sampler.stop()
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        cpu = cpu_baseline(HEADLINE)
+        cpu = cpu_baseline(HEADLINE, HEADLINE_ARGMAX)
     if rank == 0:
+        w = __import__("fp8_block_scaled_fp8blk_gb300.synth", fromlist=["WORKLOADS"]).WORKLOADS[HEADLINE]
+        nbytes = fp8blk_bytes(w["rows"], w["cols"], w["m"], HEADLINE_ARGMAX)
         line = {
             "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms / args.steps, 6),
             "us_per_call": round(us, 4), "frac_of_hbm_peak": round(per_gpu_gbs / peak, 4),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
             "data": "synthetic (seeded numpy: e4m3 codes uniform over finite codes, e8m0 2^[-8,0], x N(0,1))",
-            "config": {"workload": HEADLINE, "rows": st["rows"], "cols": st["cols"], "m": st["m"],
+            "config": {"workload": HEADLINE, "rows": w["rows"], "cols": w["cols"], "m": w["m"],
+                       "output": "one u32 greedy token per activation row (fused argmax), no logits",
                        "weights": "e4m3 codes + 128x128 f32 block scales (from e8m0)",
-                       "bytes_per_call": st["bytes"], "weight_copies": st["copies"],
-                       "l2": f"inputs larger than L2: {st['copies']} rotating weight copies "
-                             f"({st['copies'] * st['rows'] * st['cols'] / 2**20:.0f} MiB)",
-                       "timing": "CUDA graphs of back-to-back calls, CUDA events on the launch stream",
+                       "bytes_per_call": nbytes,
+                       "l2": "inputs larger than L2: rotating weight copies "
+                             f"({copies_for(w['rows'] * w['cols'])} x {w['rows'] * w['cols'] / 2**20:.0f} MiB)",
+                       "timing": f"median over {r['reps']} repetitions of exactly {args.steps} back-to-back "
+                                 "calls (CUDA graphs), CUDA events on the launch stream, barrier + device "
+                                 "synchronize around each repetition",
                        "parallelism": f"replicas x{world}"},
+            "repetitions": r["reps"],
+            "us_per_call_min_max": [round(r["ms_min"] * 1e3 / args.steps, 4), round(r["ms_max"] * 1e3 / args.steps, 4)],
             "roofline": {"bound": "hbm", "achieved": round(per_gpu_gbs, 1), "peak": peak, "unit": "GB/s",
                          "frac": round(per_gpu_gbs / peak, 4), "traffic": profiled_traffic(HEADLINE),
                          "peak_source": peak_src,
-                         "kernel": kernel_name(ops, st["m"], st["rows"], st["cols"]),
-                         "algorithmic_bytes_per_launch": st["bytes"]},
+                         "kernel": kernel_name(ops, w["m"], w["rows"], w["cols"], HEADLINE_ARGMAX),
+                         "algorithmic_bytes_per_launch": nbytes},
             "e2e": e2e,
             "gpu_launches": args.steps,
+            "gpu_launches_note": f"one kernel launch per step; {args.steps} per repetition, "
+                                 f"{args.steps * r['reps']} over all repetitions",
             "clocks": clocks,
             "device_status": status,
             "kernel_source_hash": source_hash(),
@@ -536,25 +602,19 @@ def run_reference(args):
     cores = os.cpu_count() or 1
     oracle.build()
     t0 = time.perf_counter()
-    oracle.fp8blk_gemv(case.codes[:128], case.scale_e8m0[:1], case.x, nthreads=cores)
-    per_row = (time.perf_counter() - t0) / 128
+    oracle.fp8blk_gemv(case.codes[:1024], case.scale_e8m0[:8], case.x, nthreads=cores)
+    per_row = (time.perf_counter() - t0) / 1024
     budget = 90.0 / max(1, args.steps + args.warmup)
-    sample_rows = int(min(rows, max(1, budget / max(per_row, 1e-9))))
-    if sample_rows >= 128:
-        sample_rows -= sample_rows % 128
-    nblk = math.ceil(rows / 128)
+    sample_rows = int(min(rows, max(128, budget / max(per_row, 1e-9))))
+    sample_rows -= sample_rows % 128
 
     def step(i):
-        b = i % nblk
-        r0 = b * 128
-        if sample_rows >= 128:
-            r0 = (i * sample_rows) % rows
-            r0 -= r0 % 128
-            r1 = min(rows, r0 + sample_rows)
-        else:
-            r1 = r0 + sample_rows
-        oracle.fp8blk_gemv(case.codes[r0:r1], case.scale_e8m0[r0 // 128:math.ceil(r1 / 128)], case.x,
-                           nthreads=cores)
+        r0 = (i * sample_rows) % rows
+        r0 -= r0 % 128
+        r1 = min(rows, r0 + sample_rows)
+        y, _ = oracle.fp8blk_gemv(case.codes[r0:r1], case.scale_e8m0[r0 // 128:math.ceil(r1 / 128)], case.x,
+                                  nthreads=cores)
+        oracle.argmax(y[0])
         return r1 - r0
 
     for i in range(args.warmup):
@@ -566,7 +626,7 @@ def run_reference(args):
     el = time.perf_counter() - t0
     per_step_rows = done / args.steps
     nbytes = per_step_rows * cols + math.ceil(per_step_rows / 128) * math.ceil(cols / 128) * 4 \
-        + m * cols * 4 + m * per_step_rows * 4
+        + m * cols * 4 + m * 4
     value = nbytes * args.steps / el / 1e9
     line = {
         "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": world,
@@ -577,7 +637,7 @@ def run_reference(args):
                    "sample_rows_per_step": sample_rows},
         "impl": "reference",
         "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
-                         "sample": f"{sample_rows} of {rows} rows per step, {args.steps} steps"},
+                         "sample": f"{sample_rows} of {rows} rows (+ their argmax) per step, {args.steps} steps"},
         "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
@@ -607,8 +667,8 @@ def run_profile_workload(args):
 def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=200000)
-    ap.add_argument("--warmup", type=int, default=2000)
+    ap.add_argument("--steps", type=int, default=200, help="calls per timed repetition")
+    ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--no-extra", action="store_true", help="skip the other workloads")
     ap.add_argument("--no-cpu-baseline", action="store_true")
