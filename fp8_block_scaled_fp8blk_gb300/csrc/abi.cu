@@ -198,10 +198,15 @@ Plan make_plan(int m, int64_t rows, int64_t cols, int bpw, const DeviceInfo &dev
         if (rw > 8) rw = 8;
         const int64_t warps = static_cast<int64_t>(dev.sms) * p.ctas_per_sm * kRowWarps;
         while (rw > 1 && (rows + rw - 1) / rw < warps) rw /= 2;
-        int per_warp = dev.smem_per_sm / p.ctas_per_sm - 1024 - kStaticSmemReserve;
-        const int block_cap = dev.smem_per_block - kStaticSmemReserve;
-        if (per_warp > block_cap) per_warp = block_cap;
-        per_warp /= kRowWarps;
+        int per_warp = 0;
+        for (;;) {  // fewer CTAs per SM until two one-row stages per warp fit
+            per_warp = dev.smem_per_sm / p.ctas_per_sm - 1024 - kStaticSmemReserve;
+            const int block_cap = dev.smem_per_block - kStaticSmemReserve;
+            if (per_warp > block_cap) per_warp = block_cap;
+            per_warp /= kRowWarps;
+            if (2 * panel_bytes <= per_warp || p.ctas_per_sm == 1) break;
+            --p.ctas_per_sm;
+        }
         while (rw > 1 && 2 * rw * panel_bytes > per_warp) rw /= 2;
         p.stage_rows = rw;
         p.stage_bytes = rw * panel_bytes;

@@ -146,3 +146,25 @@ def test_headline_plans(ops):
     assert p["kernel"] == 2 and p["ctas_per_sm"] == 1  # batched verify: tensor cores
     assert check_plan(ops, 4, 16384, 4096, 1)["kernel"] == 0  # m = 4: CUDA cores
     assert check_plan(ops, 8, 2048, 4096, 1)["kernel"] == 0  # small: CUDA cores
+
+
+# Launch-tuning settings (fp8blk_set_launch_tuning is public): stage sizes,
+# CTAs per SM and ring depths across their documented ranges.
+TUNINGS = [(0, 0, 1, 1, 0), (16384, 1, 1, 1, 6), (16384, 2, 1, 1, 3), (16384, 2, 1, 1, 4),
+           (32768, 1, 1, 1, 3), (32768, 1, 1, 1, 4), (65536, 1, 1, 1, 2), (16384, 3, 1, 1, 4),
+           (8192, 4, 1, 0, 2), (131072, 1, 0, 0, 8), (4096, 2, 1, 1, 8), (0, 1, 1, 1, 0),
+           (0, 2, 1, 1, 3), (16384, 2, 1, 1, 0), (65536, 1, 1, 1, 0)]
+
+
+@pytest.mark.parametrize("tuning", TUNINGS)
+def test_plans_stay_in_bounds_under_launch_tuning(ops, tuning):
+    ops.set_launch_tuning(*tuning)
+    try:
+        for m1_kernel in (1, 2):
+            ops.set_m1_kernel(m1_kernel)
+            for bpw in (1, 2):
+                for m, rows, cols in SHAPES:
+                    check_plan(ops, m, rows, cols, bpw)
+    finally:
+        ops.set_m1_kernel(0)
+        ops.set_launch_tuning()
