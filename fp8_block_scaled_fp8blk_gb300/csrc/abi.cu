@@ -139,12 +139,8 @@ cudaError_t tensor_map_2d(const void *ptr, int64_t rows, int64_t cols, int elem_
 }  // namespace
 
 cudaError_t weight_tensor_map(const uint8_t *w, int64_t rows, int64_t cols, int box_rows, CUtensorMap *out) {
-    return tensor_map_2d(w, rows, cols, 1, CU_TENSOR_MAP_DATA_TYPE_UINT8, box_rows, kTcKb, CU_TENSOR_MAP_SWIZZLE_128B,
+    return tensor_map_2d(w, rows, cols, 1, CU_TENSOR_MAP_DATA_TYPE_UINT8, box_rows, kT8Kb, CU_TENSOR_MAP_SWIZZLE_128B,
                          out);
-}
-
-cudaError_t activation_tensor_map(const float *x, int m, int64_t cols, int box_cols, CUtensorMap *out) {
-    return tensor_map_2d(x, m, cols, 4, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, m, box_cols, CU_TENSOR_MAP_SWIZZLE_NONE, out);
 }
 
 static int pow2_floor(int v) {
@@ -163,23 +159,23 @@ Plan make_plan(int m, int64_t rows, int64_t cols, int bpw, const DeviceInfo &dev
     const int64_t per = (cols + panels0 - 1) / panels0;
     p.panel_cols = static_cast<int>((per + 15) / 16 * 16);
     p.panels = static_cast<int>((cols + p.panel_cols - 1) / p.panel_cols);
-    const int64_t tc_units8 = (rows + 7) / 8;
-    const int64_t tc_rows_per_cta = (tc_units8 + dev.sms - 1) / dev.sms * 8;
-    const int64_t tc_row_blocks = tc_rows_per_cta / 128 + 2;  // most a CTA can span
-    if (bpw == 1 && m >= 2 && t.tc_min_m >= 2 && m >= t.tc_min_m && cols >= kTcKb && rows * cols >= t.tc_min_bytes &&
-        tc_row_blocks <= kTcMaxRowBlocks && tc_row_blocks * ((cols + 127) / 128) <= kTcMaxSf) {
-        // Tensor-core kernel: one CTA per SM, whole 8-row units per CTA,
-        // column panels of at most kTcMaxPanel (a multiple of kTcKb).
+    const int64_t tc_bytes = t.tc_min_bytes > 0 ? t.tc_min_bytes : tc_default_min_bytes(m);
+    // m = 1 forced onto a CUDA-core kernel (fp8blk_set_m1_kernel) skips the tensor cores.
+    const bool m1_forced = m == 1 && t.m1_kernel != 0;
+    if (bpw == 1 && !m1_forced && t.tc_min_m <= FP8BLK_MAX_M && m >= t.tc_min_m && cols >= kT8Kb &&
+        cols <= static_cast<int64_t>(kT8MaxKb) * kT8Kb && rows * cols >= tc_bytes) {
+        // Tensor-core kernel: one CTA per SM over whole 128-row tiles (one
+        // scale row block each), every K-block of a row in one pass.
         p.kind = kTensorCoreKernel;
-        p.panels = static_cast<int>((cols + kTcMaxPanel - 1) / kTcMaxPanel);
-        p.panel_cols = p.panels == 1 ? static_cast<int>(cols) : kTcMaxPanel;
+        p.panels = 1;
+        p.panel_cols = static_cast<int>(cols);
         p.team_warps_log2 = 0;
         p.rb = 1;
-        p.stage_rows = kTcM;
-        p.stage_bytes = kTcETileBytes;
-        p.stages = kTcEStages;
+        p.stage_rows = 128;
+        p.stage_bytes = kT8StageBytes;
+        p.stages = kT8Stages;
         p.ctas_per_sm = 1;
-        p.n_groups = (rows + 7) / 8;
+        p.n_groups = (rows + 127) / 128;
         return p;
     }
     const bool use_rowwarp =
@@ -563,7 +559,7 @@ int fp8blk_set_wait_limit(int64_t limit_ns) {
 }
 
 int fp8blk_set_tensor_core_min_m(int min_m, int64_t min_bytes) {
-    if (min_m != 0 && (min_m < 2 || min_m > FP8BLK_MAX_M + 1)) return FP8BLK_EINVAL;
+    if (min_m != 0 && (min_m < 1 || min_m > FP8BLK_MAX_M + 1)) return FP8BLK_EINVAL;
     if (min_bytes < 0) return FP8BLK_EINVAL;
     tuning().tc_min_m = min_m == 0 ? Tuning().tc_min_m : min_m;
     tuning().tc_min_bytes = min_bytes == 0 ? Tuning().tc_min_bytes : min_bytes;
@@ -593,7 +589,7 @@ int fp8blk_plan_query(int m, int64_t rows, int64_t cols, int bytes_per_weight, i
     out[0] = p.panels;
     out[1] = p.panel_cols;
     out[2] = p.kind == kTeamKernel ? team_warps : 1;
-    out[3] = p.kind == kRowWarpKernel ? kRowWarps : (p.kind == kTensorCoreKernel ? kTcConvWarps : kWarps / team_warps);
+    out[3] = p.kind == kRowWarpKernel ? kRowWarps : (p.kind == kTensorCoreKernel ? kT8BWarps : kWarps / team_warps);
     out[4] = p.rb;
     out[5] = p.kind == kTeamKernel ? 8 / pow2_ceil(m) : 1;
     out[6] = p.stage_rows;

@@ -8,7 +8,7 @@
 
 #include "rowwarp_gemv.cuh"
 #include "stream_gemv.cuh"
-#include "tc_gemv.cuh"
+#include "tc8_gemv.cuh"
 
 namespace fp8blk {
 
@@ -21,8 +21,8 @@ struct Tuning {
     int l2_prefetch = 1;                 // L2 prefetch of the first stages before the PDL wait
     int max_stages = kMaxStages;
     int m1_kernel = 0;                   // m = 1: 0 = by size, 1 = row-per-warp, 2 = team
-    int tc_min_m = 5;                    // tensor-core kernel for m >= this (9 = never)
-    int64_t tc_min_bytes = 32ll << 20;   // ... and at least this many weight bytes
+    int tc_min_m = 1;                    // tensor-core kernel for m >= this (9 = never)
+    int64_t tc_min_bytes = 0;            // ... and at least this many weight bytes (0 = by m, below)
     int64_t m1_rowwarp_min_bytes = 96ll << 20;  // by size: row-per-warp from this many weight bytes
     uint64_t wait_limit_ns = kWaitLimitNs;      // consumer waits of the CUDA-core kernels
 };
@@ -34,6 +34,14 @@ struct DeviceInfo {
     int smem_per_block = 0;   // opt-in maximum, bytes
     unsigned int *status = nullptr;  // device address of the status word
 };
+// Default weight-byte threshold of the tensor-core kernel by activation rows
+// (measured crossovers against the CUDA-core kernels at 4096 columns; below
+// them the tensor-core kernel's per-tile set-up and the tile count's
+// quantisation over the SMs cost more than it saves).
+inline int64_t tc_default_min_bytes(int m) {
+    return m >= 5 ? (24ll << 20) : (m >= 2 ? (48ll << 20) : (128ll << 20));
+}
+
 // Per-device facts, queried once per device (current device).
 cudaError_t current_device_info(DeviceInfo *out);
 
@@ -61,12 +69,9 @@ Plan make_plan(int m, int64_t rows, int64_t cols, int bpw, const DeviceInfo &dev
 void apply_plan(const Plan &p, GemvArgs *a);
 
 // Tensor map of an e4m3 weight matrix for the tensor-core kernel: 2-D,
-// {cols, rows}, boxes of box_rows rows x 128 bytes, 128-byte swizzle.  Cached
-// per (pointer, shape, box height).
+// {cols, rows}, boxes of box_rows rows x 128 bytes, 128-byte swizzle, zeros
+// out of range.  Cached per (pointer, shape, box height).
 cudaError_t weight_tensor_map(const uint8_t *w, int64_t rows, int64_t cols, int box_rows, CUtensorMap *out);
-// Tensor map of the m x cols f32 activations: boxes of all m rows x box_cols
-// columns, no swizzle, zeros out of range.  Cached per (pointer, m, cols).
-cudaError_t activation_tensor_map(const float *x, int m, int64_t cols, int box_cols, CUtensorMap *out);
 
 // Kernel launches (defined in gemv_e4m3.cu / gemv_bf16.cu / nvfp4_dequant.cu /
 // gemv_tc.cu).
@@ -109,7 +114,7 @@ cudaError_t launch_fp4_expert_gemv(Nvfp4Args a, bool mxfp4, const DeviceInfo &de
 
 // Dynamic shared memory of a planned launch.
 inline size_t plan_smem_bytes(const Plan &p) {
-    if (p.kind == kTensorCoreKernel) return kTcSmemBytes;
+    if (p.kind == kTensorCoreKernel) return kT8SmemBytes;
     if (p.kind == kRowWarpKernel) return static_cast<size_t>(kRowWarps) * p.stages * p.stage_bytes;
     return static_cast<size_t>(p.stages) * p.stage_bytes;
 }

@@ -299,27 +299,29 @@ int fp8blk_set_wait_limit(int64_t limit_ns);
 /*
  * fp8blk_set_m1_kernel -- which kernel serves m = 1 (speed only; results are
  * identical to within the stated error bound, and bit-identical run to run):
- *   choice 0 = by size (row-per-warp when rows * cols * bytes_per_weight >=
- *   rowwarp_min_bytes, 0 = default 96 MiB; the team kernel below), 1 = always
- *   row-per-warp, 2 = always the team kernel.  Errors: EINVAL.
+ *   choice 0 = by size (e4m3 from the tensor-core threshold of
+ *   fp8blk_set_tensor_core_min_m, 128 MiB by default: the tensor-core kernel;
+ *   below it, row-per-warp when rows * cols * bytes_per_weight >=
+ *   rowwarp_min_bytes, 0 = default 96 MiB; the team kernel below that),
+ *   1 = always row-per-warp, 2 = always the team kernel (both skip the tensor
+ *   cores).  Errors: EINVAL.
  */
 int fp8blk_set_m1_kernel(int choice, int64_t rowwarp_min_bytes);
 
 /*
  * fp8blk_set_tensor_core_min_m -- route e4m3 GEMVs with m >= min_m activation
- * rows (2..8; 9 = never; 0 = the library default, 5) and at least min_bytes
- * of weights (rows * cols; 1 = any size; 0 = the library default, 32 MiB) to
- * the tensor-core kernel ("Struct Dsv4Gpu" page,
- * verify_batch_dev: the k+1 rows of a speculative verify).  That kernel
- * re-encodes each 128 x 128 weight tile as f16 (e4m3 value times the block
- * scale, exact after a per-128-row power-of-two offset), splits x into two
- * f16 planes (about 22 significant bits) and accumulates on the tensor cores
- * in f32.  The result stays within the e4m3 GEMV error bound but is not
- * bit-identical to the CUDA-core kernels.  Row blocks whose scales are not
- * positive finite powers of two, or span more than 2^22, are computed by a
- * CUDA-core loop in the same launch.  Speed only; process-wide; not
- * thread-safe against concurrent calls of the other entry points.
- * Errors: EINVAL.
+ * rows (1..8; 9 = never; 0 = the library default, 1) and at least min_bytes
+ * of weights (rows * cols; 1 = any size; 0 = the library default, which
+ * depends on m: 24 MiB for m >= 5, 48 MiB for m = 2..4, 128 MiB for m = 1) to
+ * the tensor-core kernel ("Struct Dsv4Gpu" page, verify_batch_dev: the k+1
+ * rows of a speculative verify; decode_step_greedy: the vocab head).  That
+ * kernel feeds the stored e4m3 codes to the tensor cores unchanged, splits
+ * x * S (S the 128-row tile's block scale) into five e4m3 planes with one
+ * exponent per activation row and tile, and accumulates in f32 in tensor
+ * memory.  The result stays within the e4m3 GEMV error bound but is not
+ * bit-identical to the CUDA-core kernels.  Only for 128 <= cols <= 32768.
+ * Speed only; process-wide; not thread-safe against concurrent calls of the
+ * other entry points.  Errors: EINVAL.
  */
 int fp8blk_set_tensor_core_min_m(int min_m, int64_t min_bytes);
 

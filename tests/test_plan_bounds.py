@@ -10,8 +10,6 @@ import pytest
 GB300 = dict(sms=152, smem_per_sm=233472, smem_per_block=232448)
 STATIC_SMEM = 4736 + 128  # team kernel: red/argmax buffers, barriers, counters (ptxas report)
 ROWWARP_STATIC_SMEM = 1024  # row-per-warp kernel: barriers + argmax scratch
-TC_STATIC_SMEM = 2048  # tensor-core kernel: barriers, tables, argmax scratch (ptxas report)
-TC_MAX_ROW_BLOCKS, TC_MAX_SF = 64, 4096
 MAX_GRID = 1024
 
 
@@ -52,26 +50,31 @@ def _check_partition(n_groups, workers):
     assert all(ends[i][1] == ends[i + 1][0] for i in range(workers - 1))
 
 
+T8_SMEM = 1024 + 4 * 32768 + 8 * 6144 + 8 * 256 * 4  # A ring, B operands, block-max table
+T8_STATIC_SMEM = 2048
+T8_MAX_KB = 256
+
+
 def check_tc_plan(p, m, rows, cols, bpw):
-    """Tensor-core kernel: one CTA per SM over whole 8-row units; panels of
-    4096 columns (TMA boxes start on 128-column boundaries); the CTA's scale
-    row blocks and their f16 factors must fit the shared tables."""
-    assert m >= 2 and bpw == 1 and cols >= 128
-    pc, panels = p["panel_cols"], p["panels"]
-    assert pc == (cols if panels == 1 else 4096)
-    assert (panels - 1) * pc < cols <= panels * pc
-    n_units8 = -(-rows // 8)
-    assert p["n_groups"] == n_units8 and p["ctas_per_sm"] == 1
-    grid = min(GB300["sms"], n_units8, MAX_GRID)
-    _check_partition(n_units8, grid)
-    gcols = -(-cols // 128)
+    """Tensor-core kernel: one CTA per SM over whole 128-row tiles (one scale
+    row block each), every 128-column K-block of a tile in one pass.  Every
+    tile's box starts inside the matrix (TMA y in [0, rows)) on a 128-column
+    boundary (x a multiple of 16, as TMA requires); the ring, operands and the
+    block-max table (m x K-blocks) fit the shared memory."""
+    assert bpw == 1 and 128 <= cols <= 128 * T8_MAX_KB and 1 <= m <= 8
+    assert p["panels"] == 1 and p["panel_cols"] == cols
+    n_tiles = -(-rows // 128)
+    assert p["n_groups"] == n_tiles and p["ctas_per_sm"] == 1 and p["stages"] == 4
+    assert p["dynamic_smem_bytes"] == T8_SMEM
+    assert p["dynamic_smem_bytes"] + T8_STATIC_SMEM <= GB300["smem_per_block"]
+    nkb = -(-cols // 128)
+    assert m * nkb <= 8 * T8_MAX_KB
+    assert all((kb * 128) % 16 == 0 for kb in range(nkb))
+    grid = min(GB300["sms"], n_tiles, MAX_GRID)
+    _check_partition(n_tiles, grid)
     for b in range(grid):
-        u0, u1 = b * n_units8 // grid, (b + 1) * n_units8 // grid
-        r0, r1 = u0 * 8, min(u1 * 8, rows)
-        assert r1 > r0
-        n_rb = ((r1 - 1) >> 7) - (r0 >> 7) + 1
-        assert n_rb <= TC_MAX_ROW_BLOCKS and n_rb * gcols <= TC_MAX_SF
-    assert p["dynamic_smem_bytes"] + TC_STATIC_SMEM <= GB300["smem_per_block"]
+        t0, t1 = b * n_tiles // grid, (b + 1) * n_tiles // grid
+        assert t1 > t0 and all(0 <= 128 * t < rows for t in range(t0, t1))
     return p
 
 
@@ -133,6 +136,9 @@ def test_tensor_core_plans_stay_in_bounds(ops):
             p = check_plan(ops, m, rows, cols, 1)
             seen += p["kernel"] == 2
         assert seen > 100
+        ops.set_tensor_core_min_m(1, 1)  # m = 1 too
+        for m, rows, cols in SHAPES:
+            check_plan(ops, m, rows, cols, 1)
     finally:
         ops.set_tensor_core_min_m(0, 0)
 
@@ -141,11 +147,19 @@ def test_headline_plans(ops):
     p = check_plan(ops, 1, 4096, 4096, 1)
     assert p["panels"] == 1 and p["kernel"] == 0  # small: team kernel
     p = check_plan(ops, 1, 131072, 4096, 1)
-    assert p["kernel"] == 1  # large: row-per-warp
+    assert p["kernel"] == 2  # the vocab head: tensor cores
+    assert check_plan(ops, 1, 28672, 4096, 1)["kernel"] == 1  # 112 MiB: row-per-warp
+    ops.set_m1_kernel(1)
+    try:
+        assert check_plan(ops, 1, 131072, 4096, 1)["kernel"] == 1  # forced: row-per-warp
+    finally:
+        ops.set_m1_kernel(0)
     p = check_plan(ops, 8, 16384, 4096, 1)
     assert p["kernel"] == 2 and p["ctas_per_sm"] == 1  # batched verify: tensor cores
-    assert check_plan(ops, 4, 16384, 4096, 1)["kernel"] == 0  # m = 4: CUDA cores
+    assert check_plan(ops, 4, 16384, 4096, 1)["kernel"] == 2  # m = 4 at 64 MiB: tensor cores
+    assert check_plan(ops, 4, 8192, 4096, 1)["kernel"] == 0  # m = 4 at 32 MiB: CUDA cores
     assert check_plan(ops, 8, 2048, 4096, 1)["kernel"] == 0  # small: CUDA cores
+    assert check_plan(ops, 1, 4096, 4096, 1)["kernel"] == 0  # 16 MiB m = 1: team kernel
 
 
 # Launch-tuning settings (fp8blk_set_launch_tuning is public): stage sizes,

@@ -1,14 +1,14 @@
-"""GPU parity of the tensor-core e4m3 GEMV (m >= 2, forced on) against the
-CPU oracle, through the C ABI.
+"""GPU parity of the tensor-core e4m3 GEMV (forced on) against the CPU
+oracle, through the C ABI.
 
-The kernel re-encodes each weight tile as exact f16 (e4m3 value times the
-block scale times a per-128-row power of two), splits x into two f16 planes
-and accumulates on the tensor cores in f32.  Bar: the same per-element bound as
-the CUDA-core kernels, |gpu - oracle| <= 1e-5 * sum_c |w x| + 1e-6; bit-exact
-invariants where the encoding makes them exact (one-hot x, negation,
-power-of-two scaling of x or of the whole scale grid, run-to-run); the
-CUDA-core fallback for scale grids the f16 encoding cannot carry; the fused
-argmax.
+The kernel feeds the stored e4m3 codes to kind::f8f6f4 MMAs unchanged and
+splits x * S (S the tile's block scale, one exponent per activation row and
+128-row tile) into five e4m3 planes, accumulating in f32 in tensor memory.
+Bar: the same per-element bound as the CUDA-core kernels, |gpu - oracle| <=
+1e-5 * sum_c |w x| + 1e-6; bit-exact invariants where the encoding makes them
+exact (one-hot x, negation, power-of-two scaling of x or of the whole scale
+grid, run-to-run); wide scale spreads and scales that are not powers of two
+(they round once in f32); the fused argmax.
 """
 import numpy as np
 import pytest
@@ -57,7 +57,7 @@ def test_tc_plan_selected(ops):
     out = ops.plan_query(8, 16384, 4096, bytes_per_weight=1)
     assert out["kernel"] == TC_KIND
     assert ops.plan_query(8, 300, 16, bytes_per_weight=1)["kernel"] != TC_KIND
-    assert ops.plan_query(1, 16384, 4096, bytes_per_weight=1)["kernel"] != TC_KIND
+    assert ops.plan_query(1, 16384, 4096, bytes_per_weight=1)["kernel"] != TC_KIND  # m = 1 not forced here
 
 
 @pytest.mark.parametrize("m,rows,cols", SHAPES)
@@ -76,8 +76,9 @@ def test_tc_verify_16384x4096_m8_full(ops):
 
 
 def test_tc_x_wide_dynamic_range(ops):
-    """x spanning 2^-60 .. 2^60 within one row: the f16 planes are scaled per
-    activation row, so small elements lose at most 2^-40 of the row maximum."""
+    """x spanning 2^-60 .. 2^60 within one row: the planes are scaled per
+    activation row and tile, so small elements lose at most 2^-33 of the tile
+    maximum, far inside the bound relative to sum |w x|."""
     rows, cols, m = 640, 4096, 4
     case = synth.fp8blk_case(rows, cols, m, seed=77)
     rng = np.random.default_rng(78)
@@ -88,10 +89,9 @@ def test_tc_x_wide_dynamic_range(ops):
 
 
 def test_tc_scale_spread_at_limit_and_beyond(ops):
-    """Within a 128-row block a scale spread of 2^22 still runs on the tensor
-    cores (weights down to 2^-24 stay exact f16); 2^23 and beyond take the
-    CUDA-core fallback.  Both must match the oracle, with blocks of either kind
-    in one launch."""
+    """Block scales spread over 2^22, 2^190 and 2^-97 .. 2^93 within single
+    128-row blocks: x * S stays within f32 and the planes follow the tile's
+    largest |x S|, so every row must still match the oracle."""
     rows, cols, m = 2048, 1024, 3
     case = synth.fp8blk_case(rows, cols, m, seed=79)
     g = case.scale_e8m0
@@ -106,10 +106,10 @@ def test_tc_scale_spread_at_limit_and_beyond(ops):
     assert_close(y, ref, a, "tc scale spread")
 
 
-def test_tc_non_power_of_two_scales_take_fallback(ops):
-    """Scales passed as arbitrary f32 (not e8m0): the f16 encoding is not
-    exact, so those blocks take the CUDA-core loop; checked against the plain
-    definition sum_c w[r][c] * S[r/128][c/128] * x[i][c] in double."""
+def test_tc_non_power_of_two_scales(ops):
+    """Scales passed as arbitrary f32 (not e8m0): x * S rounds once in f32;
+    checked against the plain definition sum_c w[r][c] * S[r/128][c/128] *
+    x[i][c] in double."""
     rows, cols, m = 384, 512, 2
     case = synth.fp8blk_case(rows, cols, m, seed=80)
     sf = ops.fp8blk_scales_from_e8m0(case.scale_e8m0).copy()
@@ -185,6 +185,28 @@ def test_tc_argmax_ties_resolve_to_lowest_index(ops):
     ws = ops.argmax_workspace(m, rows, cols, "cuda:0")
     tok = ops.fp8blk_gemv_argmax(w, s, x, ws).cpu().numpy().view(np.uint32)
     assert list(tok) == [9, 9]
+
+
+@pytest.mark.parametrize("rows,cols", [(300, 400), (1000, 4096), (40000, 1040), (131, 8208)])
+def test_tc_m1_matches_oracle_and_argmax(ops, rows, cols):
+    """m = 1 on the tensor cores (the vocab head's kernel at full size): logits
+    within the bound, the token the argmax of those logits."""
+    ops.set_tensor_core_min_m(1, 1)
+    try:
+        assert ops.plan_query(1, rows, cols, bytes_per_weight=1)["kernel"] == TC_KIND
+        case = synth.fp8blk_case(rows, cols, 1, seed=rows + cols + 5)
+        w, s, x = to_dev(case.codes), scales_dev(case.scale_e8m0), to_dev(case.x)
+        ws = ops.argmax_workspace(1, rows, cols, "cuda:0")
+        logits = torch.empty((1, rows), dtype=torch.float32, device="cuda:0")
+        tok = ops.fp8blk_gemv_argmax(w, s, x, ws, logits=logits).cpu().numpy().view(np.uint32)
+        lg = logits.cpu().numpy()
+        ref, a = oracle.fp8blk_gemv(case.codes, case.scale_e8m0, case.x, nthreads=16)
+        assert_close(lg, ref, a, f"tc m=1 {rows}x{cols}")
+        assert tok[0] == oracle.argmax(lg[0].astype(np.float64))
+        y = ops.fp8blk_gemv(w, s, x).cpu().numpy()
+        assert np.array_equal(y.view(np.uint32), lg.view(np.uint32))
+    finally:
+        ops.set_tensor_core_min_m(2, 1)
 
 
 def test_tc_device_status_clean(ops):
