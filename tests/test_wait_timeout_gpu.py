@@ -27,6 +27,7 @@ def ops():
     yield o
     o.set_wait_limit()
     o.set_m1_kernel(0, 0)
+    o.set_tensor_core_min_m(0, 0)
     o.fp8blk_device_status(clear=True)
 
 
@@ -59,6 +60,7 @@ def _zero_limit_runs(ops, call, check_exact, attempts):
                                                              ("rowwarp", 1, 16384, 4096, False)])
 def test_gemv_argmax_gives_up_then_recovers(ops, kernel, m, rows, cols, must_give_up):
     ops.set_m1_kernel(1 if kernel == "rowwarp" else 2, 0)
+    ops.set_tensor_core_min_m(9, 0)  # the CUDA-core kernels take the configurable limit
     try:
         assert ops.plan_query(m, rows, cols)["kernel"] == (1 if kernel == "rowwarp" else 0)
         c = synth.fp8blk_case(rows, cols, m, seed=77)
@@ -85,6 +87,7 @@ def test_gemv_argmax_gives_up_then_recovers(ops, kernel, m, rows, cols, must_giv
         assert np.array_equal(logits.cpu().numpy().view(np.uint32), ref_logits.view(np.uint32))
     finally:
         ops.set_m1_kernel(0, 0)
+        ops.set_tensor_core_min_m(0, 0)
 
 
 def test_fp4_expert_gemv_gives_up_then_recovers(ops):
