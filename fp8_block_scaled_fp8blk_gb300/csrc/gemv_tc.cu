@@ -15,6 +15,7 @@ static cudaError_t launch_tc8(const GemvArgs &a, const Plan &p, int m, const Dev
     if (err != cudaSuccess) return err;
     if (per_sm < 1) return cudaErrorInvalidConfiguration;
     T8Args t = {};
+    t.w = a.w;
     t.scales = a.scales;
     t.x = a.x;
     t.y = a.y;
@@ -27,6 +28,7 @@ static cudaError_t launch_tc8(const GemvArgs &a, const Plan &p, int m, const Dev
     t.cols = a.cols;
     t.m = m;
     t.n_tiles = p.n_groups;
+    t.l2_prefetch = tuning().l2_prefetch ? tuning().tc_l2_prefetch : 0;
     int64_t grid = dev.sms;
     if (grid > t.n_tiles) grid = t.n_tiles;
     if (grid > kMaxGrid) grid = kMaxGrid;

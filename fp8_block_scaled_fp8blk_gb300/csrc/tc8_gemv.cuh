@@ -57,6 +57,7 @@ constexpr int kT8MmaWarp = kT8ProducerWarp + 1;   // issues K-block 0 of every s
 constexpr int kT8MmaWarps = kT8KbPerStage;
 constexpr int kT8Threads = (kT8MmaWarp + kT8MmaWarps) * 32;
 constexpr int kT8PrepassRound = 18;                // block maxima in flight per warp
+constexpr int64_t kT8PrefetchChunk = 32768;         // bytes per L2 prefetch instruction
 constexpr int kT8TileBytes = 128 * kT8Kb;                 // 16 KiB per K-block
 constexpr int kT8StageBytes = kT8KbPerStage * kT8TileBytes;
 constexpr int kT8MaxN = 48;
@@ -73,6 +74,7 @@ __host__ __device__ constexpr int t8_tmem_cols(int n) {
 }
 
 struct T8Args {
+    const uint8_t *w;        // e4m3 codes [rows, cols] (what the tensor map describes)
     const float *scales;     // f32 grid [ceil(rows/128), ceil(cols/128)]
     const float *x;          // [m, cols]
     float *y;                // [m, rows] or null (argmax only)
@@ -84,6 +86,7 @@ struct T8Args {
     int64_t rows, cols;
     int m;
     int64_t n_tiles;         // ceil(rows / 128)
+    int64_t l2_prefetch;     // bytes of the CTA's first rows prefetched into L2 at entry (0: none)
 };
 
 // UMMA shared-memory descriptor: K-major, 128-byte swizzle, 8-row groups
@@ -241,6 +244,20 @@ __global__ void __launch_bounds__(kT8Threads, 1)
     const int nst = (nkb + kT8KbPerStage - 1) / kT8KbPerStage;   // stages per tile
     const int64_t n_stages = static_cast<int64_t>(n_tiles) * nst;
     const int64_t gcols = nkb;
+
+    // The CTA's first weight rows go to L2 at entry, in address order (codes
+    // are never outputs of the preceding kernel): HBM streams through the
+    // prologue instead of idling with the ring full.  More than about a
+    // prologue's worth of streaming crowds out the other CTAs' first stages.
+    if (warp == kT8ProducerWarp && lane == 0 && a.l2_prefetch > 0 && n_tiles > 0) {
+        const int64_t r0 = T0 * 128, r1 = T1 * 128 < a.rows ? T1 * 128 : a.rows;
+        int64_t bytes = (r1 - r0) * a.cols;
+        if (bytes > a.l2_prefetch) bytes = a.l2_prefetch;
+        bytes &= ~static_cast<int64_t>(15);
+        for (int64_t off = 0; off < bytes; off += kT8PrefetchChunk)
+            bulk_prefetch_l2(a.w + r0 * a.cols + off,
+                             static_cast<uint32_t>(bytes - off < kT8PrefetchChunk ? bytes - off : kT8PrefetchChunk));
+    }
 
     if (tid == 0) {
         for (int s = 0; s < kT8Stages; ++s) {
