@@ -179,9 +179,13 @@ __device__ __forceinline__ float4 t8_ld_f32x4(const float *p) {
     return v;
 }
 
-// max that keeps NaN (fmaxf drops it).
-__device__ __forceinline__ float t8_max_nan(float a, float b) {
-    return (a != a || b != b) ? __int_as_float(0x7FC00000) : fmaxf(a, b);
+// max |v| over a warp's 128 values (4 per lane), as f32 bits.  With the sign
+// cleared, the unsigned order of f32 bits is the numeric order and every NaN
+// sorts above +inf, so a NaN anywhere is what comes out.
+__device__ __forceinline__ uint32_t t8_absmax_bits(const float4 &v) {
+    const uint32_t a = __float_as_uint(fabsf(v.x)), b = __float_as_uint(fabsf(v.y));
+    const uint32_t c = __float_as_uint(fabsf(v.z)), d = __float_as_uint(fabsf(v.w));
+    return __reduce_max_sync(0xFFFFFFFFu, max(max(a, b), max(c, d)));
 }
 
 // Single-thread wait for phase `parity`: the hinted try_wait suspends the
@@ -347,13 +351,9 @@ __global__ void __launch_bounds__(kT8Threads, 1)
             }
 #pragma unroll
             for (int j = 0; j < kT8PrepassRound; ++j) {
-                float mx = fmaxf(fmaxf(fabsf(v[j].x), fabsf(v[j].y)), fmaxf(fabsf(v[j].z), fabsf(v[j].w)));
-                const bool nan = v[j].x != v[j].x || v[j].y != v[j].y || v[j].z != v[j].z || v[j].w != v[j].w;
-#pragma unroll
-                for (int off = 16; off >= 1; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, off));
-                if (__any_sync(0xFFFFFFFFu, nan)) mx = __int_as_float(0x7FC00000);  // NaN is kept
+                const uint32_t mx = t8_absmax_bits(v[j]);
                 const int blk = b0 + j * nw;
-                if (lane == 0 && blk < nblk) sM[blk] = mx;  // row-major: blk = i * nkb + kb
+                if (lane == 0 && blk < nblk) sM[blk] = __uint_as_float(mx);  // row-major: blk = i * nkb + kb
             }
             bkb = kbj;
             bi = ij;
@@ -380,9 +380,9 @@ __global__ void __launch_bounds__(kT8Threads, 1)
     // given the tile's scale row (warp-collective; every builder and epilogue
     // warp computes the same bits).
     auto tile_exponents = [&](const float (&sc)[kT8MaxKb / 32], int (&ex)[8]) {
-        float gi[8];
+        uint32_t gi[8];  // f32 bits of non-negative values (or NaN): ordered as unsigned
 #pragma unroll
-        for (int i = 0; i < 8; ++i) gi[i] = 0.f;
+        for (int i = 0; i < 8; ++i) gi[i] = 0u;
 #pragma unroll
         for (int j = 0; j < kT8MaxKb / 32; ++j) {
             const int kb = lane + 32 * j;
@@ -390,15 +390,11 @@ __global__ void __launch_bounds__(kT8Threads, 1)
                 const float s_abs = fabsf(sc[j]);
 #pragma unroll
                 for (int i = 0; i < 8; ++i)
-                    if (i < m) gi[i] = t8_max_nan(gi[i], s_abs * sM[i * nkb + kb]);
+                    if (i < m) gi[i] = max(gi[i], __float_as_uint(fabsf(s_abs * sM[i * nkb + kb])));
             }
         }
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-#pragma unroll
-            for (int off = 16; off >= 1; off >>= 1) gi[i] = t8_max_nan(gi[i], __shfl_xor_sync(0xFFFFFFFFu, gi[i], off));
-            ex[i] = t8_plane_exponent(gi[i]);
-        }
+        for (int i = 0; i < 8; ++i) ex[i] = t8_plane_exponent(__uint_as_float(__reduce_max_sync(0xFFFFFFFFu, gi[i])));
     };
 
     float best_v[8];
