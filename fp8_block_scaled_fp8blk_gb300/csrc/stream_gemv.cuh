@@ -273,6 +273,20 @@ __device__ __forceinline__ void warp_argmax_merge(float &v, uint32_t &i) {
     }
 }
 
+// Warp-wide greedy argmax, every lane ending with the warp's best: one
+// redux.sync takes the largest order key, a second the lowest index among the
+// lanes holding it.  The key orders floats as argmax_better compares them
+// (-0 as +0); NaN, which argmax_better never prefers, is never a lane's best
+// (each starts from -inf), so it needs no key.  Same result as the shuffle
+// tree of warp_argmax_merge<1>, in two instructions instead of ten.
+__device__ __forceinline__ void warp_argmax_all(float &v, uint32_t &i) {
+    const uint32_t b = __float_as_uint(v + 0.0f);  // -0 -> +0
+    const uint32_t key = (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+    const uint32_t kmax = __reduce_max_sync(0xFFFFFFFFu, key);
+    i = __reduce_min_sync(0xFFFFFFFFu, key == kmax ? i : 0xFFFFFFFFu);
+    v = __uint_as_float((kmax & 0x80000000u) ? (kmax & 0x7FFFFFFFu) : ~kmax);
+}
+
 constexpr int kAmWarps = 16;  // rows of the argmax merge scratch (one per warp)
 
 // Called by every thread of the CTA after its per-activation-row partials
@@ -303,7 +317,7 @@ __device__ __forceinline__ void argmax_cross_cta(const GemvArgs &a, float (&am_v
                 ix = ci;
             }
         }
-        warp_argmax_merge<1>(v, ix);
+        warp_argmax_all(v, ix);
         __syncthreads();
         if (lane == 0) {
             am_val[warp][0] = v;

@@ -600,13 +600,16 @@ __global__ void __launch_bounds__(kT8Threads, 1)
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(t8_tmem_cols(N)) : "memory");
 
     if constexpr (ARGMAX) {
+#pragma unroll
         for (int i = 0; i < 8; ++i) {
-            float bv = best_v[i];
-            uint32_t bi = best_i[i];
-            warp_argmax_merge<1>(bv, bi);
-            if (lane == 0) {
-                am_val[warp][i] = bv;
-                am_idx[warp][i] = bi;
+            if (i < m) {
+                float bv = best_v[i];
+                uint32_t bi = best_i[i];
+                warp_argmax_all(bv, bi);
+                if (lane == 0) {
+                    am_val[warp][i] = bv;
+                    am_idx[warp][i] = bi;
+                }
             }
         }
         __syncthreads();
