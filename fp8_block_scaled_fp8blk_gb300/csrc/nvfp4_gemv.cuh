@@ -63,17 +63,31 @@ __device__ __forceinline__ int nv_expert(const Nvfp4Args &a, int k, float *g) {
     return e;
 }
 
+// The expert of the slot last looked up: a warp's units run through few
+// slots, and each lookup is two dependent global loads.
+struct NvSlot {
+    int k = -1, e = -1;
+    float g = 0.f;
+};
+template <int FP4>
+__device__ __forceinline__ const NvSlot &nv_slot(const Nvfp4Args &a, int k, NvSlot &c) {
+    if (k != c.k) {
+        c.k = k;
+        c.e = nv_expert<FP4>(a, k, &c.g);
+    }
+    return c;
+}
+
 // Lane 0: copy unit u (slot k, row group, panel) into a ring stage.
 template <int FP4>
 __device__ __forceinline__ void nv_issue(const Nvfp4Args &a, int64_t u, int64_t n_my, int64_t g0,
-                                         uint32_t dst, uint32_t bar, uint64_t policy) {
+                                         uint32_t dst, uint32_t bar, uint64_t policy, NvSlot &cache) {
     const int panel = static_cast<int>(u / n_my);
     const int64_t gg = g0 + u % n_my;  // global group index over (slot, row group)
     const int k = static_cast<int>(gg / a.groups);
     const int64_t row0 = (gg % a.groups) * a.stage_rows;
     const int nr = static_cast<int>(a.rows - row0 < a.stage_rows ? a.rows - row0 : a.stage_rows);
-    float g;
-    const int e = nv_expert<FP4>(a, k, &g);
+    const int e = nv_slot<FP4>(a, k, cache).e;
     if (e < 0) {  // nothing to copy: complete the phase so the consumers move on
         mbar_arrive(bar);
         return;
@@ -117,15 +131,25 @@ __device__ __forceinline__ void nv_load_x(const Nvfp4Args &a, int panel, int pc,
     }
 }
 
-// Single-panel shapes: the CTA loads x once (coalesced) into shared memory in
-// lane-transposed float4 order, xT[(j * 8 + q) * 32 + l] = x4[(j * 32 + l) * 8 + q],
-// so that each warp fills its registers with conflict-free 16-byte reads.
-__device__ __forceinline__ void nv_stage_x(const Nvfp4Args &a, float4 *xT) {
+// Single-panel shapes: the CTA loads x once (coalesced, every load in flight
+// at once) into shared memory in lane-transposed float4 order,
+// xT[(j * 8 + q) * 32 + l] = x4[(j * 32 + l) * 8 + q], so that each warp
+// fills its registers with conflict-free 16-byte reads.
+constexpr int kNvXPerThread = kNvMaxPanel / 4 / kNvThreads;
+__device__ __forceinline__ void nv_stage_x_load(const Nvfp4Args &a, float4 (&v)[kNvXPerThread]) {
     const int n4 = static_cast<int>(a.cols / 4);
-    for (int i = threadIdx.x; i < kNvMaxPanel / 4; i += kNvThreads) {
-        const float4 v = i < n4 ? __ldg(reinterpret_cast<const float4 *>(a.x) + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int t = 0; t < kNvXPerThread; ++t) {
+        const int i = static_cast<int>(threadIdx.x) + t * kNvThreads;
+        v[t] = i < n4 ? __ldg(reinterpret_cast<const float4 *>(a.x) + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+}
+__device__ __forceinline__ void nv_stage_x_store(const float4 (&v)[kNvXPerThread], float4 *xT) {
+#pragma unroll
+    for (int t = 0; t < kNvXPerThread; ++t) {
+        const int i = static_cast<int>(threadIdx.x) + t * kNvThreads;
         const int chunk = i >> 3, q = i & 7;
-        xT[((chunk >> 5) * 8 + q) * 32 + (chunk & 31)] = v;
+        xT[((chunk >> 5) * 8 + q) * 32 + (chunk & 31)] = v[t];
     }
 }
 
@@ -211,18 +235,23 @@ __global__ void __launch_bounds__(kNvThreads, 2) fp4_expert_gemv_kernel(const Nv
     // The ids, scales and x may be outputs of the preceding kernel.
     grid_dependency_wait();
     grid_launch_dependents();
+    // x loads first: they are in flight while lane 0 looks the experts up
+    // (dependent loads) and issues the first ring.
+    float4 xv[kNvXPerThread];
+    if (x_in_smem) nv_stage_x_load(a, xv);
     const uint64_t policy = l2_policy_evict_first();
     const int64_t first = units < stages ? units : stages;
+    NvSlot issue_slot, use_slot;
     if (lane == 0)
         for (int64_t u = 0; u < first; ++u)
             nv_issue<FP4>(a, u, n_my, g0, smem_addr(ring + u * a.stage_bytes), bar0 + 8 * static_cast<uint32_t>(u),
-                          policy);
+                          policy, issue_slot);
     int64_t issued_end = first;
 
     float xr[128];
     int cur_panel = -1;
     if (x_in_smem) {  // uniform over the CTA
-        nv_stage_x(a, xT);
+        nv_stage_x_store(xv, xT);
         __syncthreads();
         nv_load_x_smem(xT, lane, xr);
         cur_panel = 0;
@@ -242,8 +271,9 @@ __global__ void __launch_bounds__(kNvThreads, 2) fp4_expert_gemv_kernel(const Nv
             nv_load_x(a, panel, pc, lane, xr);
             cur_panel = panel;
         }
-        float g = 0.f;
-        const int e = nv_expert<FP4>(a, k, &g);
+        const NvSlot &sl = nv_slot<FP4>(a, k, use_slot);
+        const int e = sl.e;
+        const float g = sl.g;
         const bool ok = mbar_wait_limit(bar0 + 8 * s, static_cast<uint32_t>((u / stages) & 1), a.wait_limit_ns);
         if (!__all_sync(0xFFFFFFFFu, ok)) {
             aborted = true;
@@ -281,7 +311,7 @@ __global__ void __launch_bounds__(kNvThreads, 2) fp4_expert_gemv_kernel(const Nv
         if (u + stages < units) {
             if (lane == 0)
                 nv_issue<FP4>(a, u + stages, n_my, g0, smem_addr(ring + static_cast<size_t>(s) * a.stage_bytes),
-                              bar0 + 8 * s, policy);
+                              bar0 + 8 * s, policy, issue_slot);
             issued_end = u + stages + 1;
         }
     }
