@@ -136,3 +136,36 @@ def test_fused_matches_two_step_path(ops, c5):
     y1 = fused(ops, c5)
     _, a, _ = oracle.nvfp4_expert_dequant_gemv(c5.codes, c5.scales, c5.gscale, c5.ids, c5.x, nthreads=16)
     assert np.all(np.abs(y1.astype(np.float64) - y2) <= 2 * (1e-5 * a + 1e-6))
+
+
+def test_fused_x_wide_dynamic_range(ops):
+    """x spanning 2^-40 .. 2^20: the f32 sums keep the small terms' share."""
+    case = synth.nvfp4_case(3, 256, 2048, 2, seed=77)
+    rng = np.random.default_rng(78)
+    x = (rng.standard_normal(2048) * np.exp2(rng.integers(-40, 21, 2048))).astype(np.float32)
+    case = synth.Nvfp4Case(case.codes, case.scales, case.gscale, case.ids, x)
+    y = fused(ops, case)
+    ref, a, _ = oracle.nvfp4_expert_dequant_gemv(case.codes, case.scales, case.gscale, case.ids, case.x, nthreads=8)
+    assert_close(y, ref, a, "fused nvfp4 wide x")
+
+
+def test_fused_nan_scale_poisons_only_its_row(ops):
+    """An e4m3 NaN scale (0x7F) makes its 16 weights NaN: that row's output is
+    NaN, every other row is untouched."""
+    case = synth.nvfp4_case(2, 300, 1024, 2, seed=79)
+    scales = case.scales.copy()
+    e = int(case.ids[1])
+    scales[e, 133, 5] = 0x7F
+    case = synth.Nvfp4Case(case.codes, scales, case.gscale, case.ids, case.x)
+    y = fused(ops, case)
+    assert np.isnan(y[1, 133]) and np.isnan(y).sum() == 1
+    ok = np.ones_like(y, dtype=bool)
+    ok[1, 133] = False
+    ref, a, _ = oracle.nvfp4_expert_dequant_gemv(case.codes, case.scales, case.gscale, case.ids, case.x, nthreads=8)
+    assert_close(y[ok], ref[ok], a[ok], "rows next to the NaN scale")
+
+
+def test_fused_bit_identical_rerun(ops, c5):
+    """Two calls on the same inputs give the same bits (fixed reduction order)."""
+    y1, y2 = fused(ops, c5), fused(ops, c5)
+    assert np.array_equal(y1.view(np.uint32), y2.view(np.uint32))
