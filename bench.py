@@ -88,11 +88,24 @@ KERNEL_SOURCES = ("device_common.cuh", "stream_gemv.cuh", "rowwarp_gemv.cuh", "t
                   "nvfp4_gemv.cu")
 
 
-def source_hash() -> str:
-    """Hash of the kernel sources; a committed ncu traffic figure is reported
-    only while it matches (i.e. while the kernels are the ones profiled)."""
+# The sources that decide each profiled workload's dominant kernel and its
+# launch shape: a committed traffic figure stays valid while these hash the same.
+_PLAN_SOURCES = ("device_common.cuh", "launch.h", "abi.cu")
+TRAFFIC_SOURCES = {
+    "head_argmax_131072x4096_m1": _PLAN_SOURCES + ("stream_gemv.cuh", "tc8_gemv.cuh", "gemv_tc.cu"),
+    "verify_16384x4096_m8": _PLAN_SOURCES + ("stream_gemv.cuh", "tc8_gemv.cuh", "gemv_tc.cu"),
+    "gemv_4096x4096_m1": _PLAN_SOURCES + ("stream_gemv.cuh", "gemv_e4m3.cu"),
+    "nvfp4_experts_6of64_2048x4096": _PLAN_SOURCES + ("rowwarp_gemv.cuh", "nvfp4_gemv.cuh", "nvfp4_gemv.cu"),
+    "mxfp4_experts_6of64_2048x4096": _PLAN_SOURCES + ("rowwarp_gemv.cuh", "nvfp4_gemv.cuh", "nvfp4_gemv.cu"),
+}
+
+
+def source_hash(names=KERNEL_SOURCES) -> str:
+    """Hash of kernel sources (all of them by default); a committed ncu traffic
+    figure is reported only while its workload's sources match (i.e. while the
+    kernel is the one profiled)."""
     h = hashlib.sha1()
-    for name in KERNEL_SOURCES:
+    for name in names:
         with open(os.path.join(CSRC, name), "rb") as f:
             h.update(name.encode())
             h.update(f.read())
@@ -114,7 +127,9 @@ def profiled_traffic(workload: str):
     p = os.path.join(ROOT, "profiles", "ncu_traffic.txt")
     if not os.path.exists(p):
         return None
-    cur = source_hash()
+    if workload not in TRAFFIC_SOURCES:
+        return None
+    cur = source_hash(TRAFFIC_SOURCES[workload])
     with open(p) as f:
         for line in f:
             parts = line.split()
@@ -384,6 +399,15 @@ def summarize(st: dict, r: dict, steps: int, peak: float, sampler, **extra) -> d
     return out
 
 
+def with_traffic(out: dict) -> dict:
+    """Add each entry's committed ncu DRAM bytes per launch (while current)."""
+    for name, entry in out.items():
+        t = profiled_traffic(name)
+        if t is not None:
+            entry["ncu_dram_bytes_per_launch"] = t
+    return out
+
+
 def measure_extra(device, stream, world, peak, steps, warmup, sampler):
     """The other workloads of the path, timed the same way (one JSON line)."""
     from fp8_block_scaled_fp8blk_gb300 import ops
@@ -430,7 +454,7 @@ def measure_extra(device, stream, world, peak, steps, warmup, sampler):
     out["mxfp4_experts_6of64_2048x4096"] = summarize(
         st, r, steps, peak, sampler,
         note="the MTP block's OCP MXFP4 experts: one launch, e8m0 per 32 columns decoded in registers")
-    return out
+    return with_traffic(out)
 
 
 def measure_e2e(st, steps: int, device, min_seconds: float = 0.5) -> dict:
