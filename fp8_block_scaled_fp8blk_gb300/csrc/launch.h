@@ -40,7 +40,7 @@ struct DeviceInfo {
 // them the tensor-core kernel's per-tile set-up and the tile count's
 // quantisation over the SMs cost more than it saves).
 inline int64_t tc_default_min_bytes(int m) {
-    return m >= 5 ? (24ll << 20) : (m >= 2 ? (48ll << 20) : (128ll << 20));
+    return m >= 5 ? (24ll << 20) : (m >= 3 ? (32ll << 20) : (48ll << 20));
 }
 
 // Per-device facts, queried once per device (current device).

@@ -300,9 +300,10 @@ int fp8blk_set_wait_limit(int64_t limit_ns);
  * fp8blk_set_m1_kernel -- which kernel serves m = 1 (speed only; results are
  * identical to within the stated error bound, and bit-identical run to run):
  *   choice 0 = by size (e4m3 from the tensor-core threshold of
- *   fp8blk_set_tensor_core_min_m, 128 MiB by default: the tensor-core kernel;
- *   below it, row-per-warp when rows * cols * bytes_per_weight >=
- *   rowwarp_min_bytes, 0 = default 96 MiB; the team kernel below that),
+ *   fp8blk_set_tensor_core_min_m, 48 MiB by default: the tensor-core kernel;
+ *   otherwise -- below it, or a shape the tensor-core kernel does not take --
+ *   row-per-warp when rows * cols * bytes_per_weight >= rowwarp_min_bytes,
+ *   0 = default 96 MiB; the team kernel below that),
  *   1 = always row-per-warp, 2 = always the team kernel (both skip the tensor
  *   cores).  Errors: EINVAL.
  */
@@ -312,7 +313,7 @@ int fp8blk_set_m1_kernel(int choice, int64_t rowwarp_min_bytes);
  * fp8blk_set_tensor_core_min_m -- route e4m3 GEMVs with m >= min_m activation
  * rows (1..8; 9 = never; 0 = the library default, 1) and at least min_bytes
  * of weights (rows * cols; 1 = any size; 0 = the library default, which
- * depends on m: 24 MiB for m >= 5, 48 MiB for m = 2..4, 128 MiB for m = 1) to
+ * depends on m: 24 MiB for m >= 5, 32 MiB for m = 3..4, 48 MiB for m = 1..2) to
  * the tensor-core kernel ("Struct Dsv4Gpu" page, verify_batch_dev: the k+1
  * rows of a speculative verify; decode_step_greedy: the vocab head).  That
  * kernel feeds the stored e4m3 codes to the tensor cores unchanged, splits

@@ -148,7 +148,9 @@ def test_headline_plans(ops):
     assert p["panels"] == 1 and p["kernel"] == 0  # small: team kernel
     p = check_plan(ops, 1, 131072, 4096, 1)
     assert p["kernel"] == 2  # the vocab head: tensor cores
-    assert check_plan(ops, 1, 28672, 4096, 1)["kernel"] == 1  # 112 MiB: row-per-warp
+    assert check_plan(ops, 1, 28672, 4096, 1)["kernel"] == 2  # 112 MiB: tensor cores
+    assert check_plan(ops, 1, 8192, 4096, 1)["kernel"] == 0  # 32 MiB: team kernel
+    assert check_plan(ops, 1, 3072, 36864, 1)["kernel"] == 1  # 108 MiB, too wide for the tensor cores
     ops.set_m1_kernel(1)
     try:
         assert check_plan(ops, 1, 131072, 4096, 1)["kernel"] == 1  # forced: row-per-warp
@@ -157,7 +159,9 @@ def test_headline_plans(ops):
     p = check_plan(ops, 8, 16384, 4096, 1)
     assert p["kernel"] == 2 and p["ctas_per_sm"] == 1  # batched verify: tensor cores
     assert check_plan(ops, 4, 16384, 4096, 1)["kernel"] == 2  # m = 4 at 64 MiB: tensor cores
-    assert check_plan(ops, 4, 8192, 4096, 1)["kernel"] == 0  # m = 4 at 32 MiB: CUDA cores
+    assert check_plan(ops, 4, 8192, 4096, 1)["kernel"] == 2  # m = 4 at 32 MiB: tensor cores
+    assert check_plan(ops, 4, 4096, 4096, 1)["kernel"] == 0  # m = 4 at 16 MiB: CUDA cores
+    assert check_plan(ops, 2, 8192, 4096, 1)["kernel"] == 0  # m = 2 at 32 MiB: CUDA cores
     assert check_plan(ops, 8, 2048, 4096, 1)["kernel"] == 0  # small: CUDA cores
     assert check_plan(ops, 1, 4096, 4096, 1)["kernel"] == 0  # 16 MiB m = 1: team kernel
 

@@ -51,12 +51,13 @@ def _noalloc_c_abi(ops, w, s, x, m, rows, cols, with_logits):
 
 
 # Shapes that reach every kernel the fused argmax can run: the team kernel
-# (small and ragged), the row-per-warp kernel (m = 1 with 96 to 128 MiB of
-# weights), the tensor-core kernel (the 131072 x 4096 vocab head at m = 1, the
-# 16384 x 4096 verify at m = 8) and the multi-panel accumulator (cols > 4096).
+# (small and ragged), the row-per-warp kernel (m = 1 from 96 MiB of weights
+# when too wide for the tensor cores: 3072 x 36864), the tensor-core kernel
+# (28672 and 131072 rows at m = 1, the 16384 x 4096 verify at m = 8) and the
+# multi-panel accumulator (cols > 4096).
 @pytest.mark.parametrize("m,rows,cols", [(1, 20000, 4096), (3, 1000, 1040), (8, 640, 4096),
                                          (1, 28672, 4096), (1, 131072, 4096), (8, 16384, 4096),
-                                         (1, 64, 8192)])
+                                         (1, 64, 8192), (1, 3072, 36864)])
 def test_noalloc_matches_workspace_entry_point_on_two_calls(ops, m, rows, cols):
     cases = [synth.fp8blk_case(rows, cols, m, seed=900 + k) for k in range(2)]
     devs = [(to_dev(c.codes), scales_dev(c.scale_e8m0), to_dev(c.x)) for c in cases]
