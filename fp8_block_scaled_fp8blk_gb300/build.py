@@ -4,9 +4,8 @@ Compiles the translation units in ``csrc/`` in parallel and links them into
 ``_build/libfp8blk.so`` (shared CUDA runtime, so the library shares torch's
 runtime and streams).  Rebuilds only when a source or header is newer than the
 library.  Usage: ``python -m fp8_block_scaled_fp8blk_gb300.build [--force] [-v]``.
-Extra nvcc flags (e.g. ``-DTC_E_STAGES=6`` for the tensor-core kernel's ring
-depths) come from the ``FP8BLK_NVCC_EXTRA`` environment variable; changing
-them needs ``--force``.
+Extra nvcc flags (e.g. ``-lineinfo``-style diagnostics) come from the
+``FP8BLK_NVCC_EXTRA`` environment variable; changing them needs ``--force``.
 """
 from __future__ import annotations
 

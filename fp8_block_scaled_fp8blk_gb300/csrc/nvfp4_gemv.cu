@@ -3,14 +3,9 @@
 #include "launch.h"
 #include "nvfp4_gemv.cuh"
 
-#ifndef NV_STAGE_TARGET
-#define NV_STAGE_TARGET 16384
-#endif
-#ifndef NV_SHRINK
-#define NV_SHRINK 1
-#endif
-
 namespace fp8blk {
+
+constexpr int kNvStageTarget = 16384;  // bytes of two stages (R rows each) the row count aims at
 
 cudaError_t launch_fp4_expert_gemv(Nvfp4Args a, bool mxfp4, const DeviceInfo &dev, cudaStream_t stream) {
     a.panels = static_cast<int>((a.cols + kNvMaxPanel - 1) / kNvMaxPanel);
@@ -20,9 +15,9 @@ cudaError_t launch_fp4_expert_gemv(Nvfp4Args a, bool mxfp4, const DeviceInfo &de
     // groups than warps; as many stages as two CTAs per SM leave room for.
     const int ctas_per_sm = 2;
     int rw = 1;
-    while (rw < 8 && 2 * rw * row_bytes <= NV_STAGE_TARGET) rw *= 2;
+    while (rw < 8 && 2 * rw * row_bytes <= kNvStageTarget) rw *= 2;
     const int64_t warps = static_cast<int64_t>(dev.sms) * ctas_per_sm * kNvWarps;
-    while (NV_SHRINK && rw > 1 && (a.rows + rw - 1) / rw * a.n_active < warps) rw /= 2;
+    while (rw > 1 && (a.rows + rw - 1) / rw * a.n_active < warps) rw /= 2;
     a.stage_rows = rw;
     a.stage_bytes = rw * row_bytes;
     a.groups = (a.rows + rw - 1) / rw;
