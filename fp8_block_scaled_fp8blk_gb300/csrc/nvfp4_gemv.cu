@@ -12,20 +12,22 @@ cudaError_t launch_fp4_expert_gemv(Nvfp4Args a, bool mxfp4, const DeviceInfo &de
     a.panel_cols = a.panels == 1 ? static_cast<int>(a.cols) : kNvMaxPanel;
     const int row_bytes = a.panel_cols / 2 + a.panel_cols / (mxfp4 ? 32 : 16);
     // Stages of about 8 KiB (R rows), fewer rows while there are fewer row
-    // groups than warps; as many stages as two CTAs per SM leave room for.
-    const int ctas_per_sm = 2;
-    int rw = 1;
-    while (rw < 8 && 2 * rw * row_bytes <= kNvStageTarget) rw *= 2;
-    const int64_t warps = static_cast<int64_t>(dev.sms) * ctas_per_sm * kNvWarps;
-    while (rw > 1 && (a.rows + rw - 1) / rw * a.n_active < warps) rw /= 2;
-    a.stage_rows = rw;
-    a.stage_bytes = rw * row_bytes;
-    a.groups = (a.rows + rw - 1) / rw;
+    // groups than warps or while two stages per warp do not fit beside x in
+    // the CTA's share of the SM (kNvCtasPerSm CTAs per SM).
+    const int ctas_per_sm = kNvCtasPerSm;
     const int x_bytes = a.panels == 1 ? kNvXSmemBytes : 0;  // x staged once per CTA
     int per_cta = dev.smem_per_sm / ctas_per_sm - 1024 - kStaticSmemReserve;
     const int block_cap = dev.smem_per_block - kStaticSmemReserve;
     if (per_cta > block_cap) per_cta = block_cap;
     const int per_warp = (per_cta - x_bytes) / kNvWarps;
+    int rw = 1;
+    while (rw < 8 && 2 * rw * row_bytes <= kNvStageTarget) rw *= 2;
+    while (rw > 1 && per_warp / (rw * row_bytes) < 2) rw /= 2;
+    const int64_t warps = static_cast<int64_t>(dev.sms) * ctas_per_sm * kNvWarps;
+    while (rw > 1 && (a.rows + rw - 1) / rw * a.n_active < warps) rw /= 2;
+    a.stage_rows = rw;
+    a.stage_bytes = rw * row_bytes;
+    a.groups = (a.rows + rw - 1) / rw;
     int stages = per_warp / a.stage_bytes;
     if (stages > kMaxStages) stages = kMaxStages;
     if (stages < 2) return cudaErrorInvalidConfiguration;

@@ -32,7 +32,9 @@ namespace fp8blk {
 
 constexpr int kNvWarps = 4;
 constexpr int kNvThreads = kNvWarps * 32;
-constexpr int kNvMaxPanel = 4096;           // columns per panel (x for 128 columns per lane)
+constexpr int kNvMaxPanel = 4096;           // columns per panel
+constexpr int kNvChunks = kNvMaxPanel / 1024;  // 32-column chunks of a panel per lane (x registers: 32 each)
+constexpr int kNvCtasPerSm = 2;
 constexpr unsigned kStatusBadExpert = 2u;   // FP8BLK_STATUS_BAD_EXPERT
 constexpr int kFp4Nv = 0;                   // NVFP4: e4m3 scale per 16 columns, f32 global scale
 constexpr int kFp4Mx = 1;                   // MXFP4: e8m0 scale per 32 columns
@@ -114,9 +116,9 @@ __device__ __forceinline__ void nv_issue(const Nvfp4Args &a, int64_t u, int64_t 
 
 // x for this lane's chunks of the panel: chunk c = 32 columns, lane l holds
 // chunks l, l + 32, l + 64, l + 96.
-__device__ __forceinline__ void nv_load_x(const Nvfp4Args &a, int panel, int pc, int lane, float (&xr)[128]) {
+__device__ __forceinline__ void nv_load_x(const Nvfp4Args &a, int panel, int pc, int lane, float (&xr)[32 * kNvChunks]) {
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
+    for (int j = 0; j < kNvChunks; ++j) {
         const int chunk = j * 32 + lane;
         const bool ok = chunk * 32 < pc;
         const int64_t c0 = static_cast<int64_t>(panel) * a.panel_cols + static_cast<int64_t>(chunk) * 32;
@@ -153,9 +155,9 @@ __device__ __forceinline__ void nv_stage_x_store(const float4 (&v)[kNvXPerThread
     }
 }
 
-__device__ __forceinline__ void nv_load_x_smem(const float4 *xT, int lane, float (&xr)[128]) {
+__device__ __forceinline__ void nv_load_x_smem(const float4 *xT, int lane, float (&xr)[32 * kNvChunks]) {
 #pragma unroll
-    for (int j = 0; j < 4; ++j)
+    for (int j = 0; j < kNvChunks; ++j)
 #pragma unroll
         for (int q = 0; q < 8; ++q) {
             const float4 v = xT[(j * 8 + q) * 32 + lane];
@@ -185,10 +187,10 @@ __device__ __forceinline__ float nv_block16(uint32_t w0, uint32_t w1, const floa
 // block scale(s) times the sums of e2m1 * x.
 template <int FP4, bool FULL>
 __device__ __forceinline__ float nv_row(const uint8_t *crow, const uint8_t *srow, int lane, int pc,
-                                        const float (&xr)[128]) {
+                                        const float (&xr)[32 * kNvChunks]) {
     float acc = 0.f;
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
+    for (int j = 0; j < kNvChunks; ++j) {
         const int chunk = j * 32 + lane;
         if (FULL || chunk * 32 < pc) {
             const uint4 q = *reinterpret_cast<const uint4 *>(crow + chunk * 16);
@@ -207,7 +209,7 @@ __device__ __forceinline__ float nv_row(const uint8_t *crow, const uint8_t *srow
 }
 
 template <int FP4>
-__global__ void __launch_bounds__(kNvThreads, 2) fp4_expert_gemv_kernel(const Nvfp4Args a) {
+__global__ void __launch_bounds__(kNvThreads, kNvCtasPerSm) fp4_expert_gemv_kernel(const Nvfp4Args a) {
     constexpr int SC = fp4_scale_cols<FP4>();
     extern __shared__ __align__(128) uint8_t smem[];
     __shared__ __align__(8) uint64_t bars[kNvWarps][kMaxStages];
@@ -248,7 +250,7 @@ __global__ void __launch_bounds__(kNvThreads, 2) fp4_expert_gemv_kernel(const Nv
                           policy, issue_slot);
     int64_t issued_end = first;
 
-    float xr[128];
+    float xr[32 * kNvChunks];
     int cur_panel = -1;
     if (x_in_smem) {  // uniform over the CTA
         nv_stage_x_store(xv, xT);
