@@ -19,7 +19,7 @@ struct Tuning {
     int ctas_per_sm = 0;                 // 0 = 2 for m <= 4, 1 for m > 4
     int use_pdl = 1;                     // programmatic dependent launch
     int l2_prefetch = 1;                 // L2 prefetch of the first stages before the PDL wait
-    int64_t tc_l2_prefetch = 256 * 1024; // tensor-core kernel: bytes of each CTA's first rows prefetched
+    int64_t tc_l2_prefetch = 192 * 1024; // tensor-core kernel: bytes of each CTA's first rows prefetched
     int max_stages = kMaxStages;
     int m1_kernel = 0;                   // m = 1: 0 = by size, 1 = row-per-warp, 2 = team
     int tc_min_m = 1;                    // tensor-core kernel for m >= this (9 = never)

@@ -270,7 +270,7 @@ int mxfp4_expert_gemv(const uint8_t *codes, const uint8_t *scales, int n_experts
  *   use_pdl             programmatic dependent launch on (nonzero) or off
  *   l2_prefetch         L2 prefetch, before the grid dependency wait, of the
  *                       stages after the first ring (e4m3) or of the first
- *                       stages (bf16), and of each CTA's first 256 KiB of
+ *                       stages (bf16), and of each CTA's first 192 KiB of
  *                       weight rows (tensor-core kernel), on (nonzero) or off
  *   max_stages          pipeline depth cap, 2..8 (8)
  * Not thread-safe against concurrent calls of the other entry points.

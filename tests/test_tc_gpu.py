@@ -145,6 +145,26 @@ def test_tc_one_hot_exact_and_invariants(ops):
     assert np.array_equal(run(ops, codes, sf * np.float32(2.0 ** 5), xr), y0 * np.float32(2.0 ** 5))
 
 
+def test_tc_bit_identical_under_launch_tuning(ops):
+    """The entry L2 prefetch and programmatic dependent launch change timing
+    only: the tensor-core kernel's outputs and tokens keep every bit."""
+    rows, cols, m = 5000, 2064, 3
+    case = synth.fp8blk_case(rows, cols, m, seed=82)
+    w, s, x = to_dev(case.codes), scales_dev(case.scale_e8m0), to_dev(case.x)
+    ws = ops.argmax_workspace(m, rows, cols, "cuda:0")
+    lg = torch.empty((m, rows), dtype=torch.float32, device="cuda:0")
+    y0 = ops.fp8blk_gemv(w, s, x).clone()
+    t0 = ops.fp8blk_gemv_argmax(w, s, x, ws, logits=lg).clone()
+    assert torch.equal(lg, y0)
+    try:
+        for tune in (dict(l2_prefetch=0), dict(use_pdl=0), dict(l2_prefetch=0, use_pdl=0)):
+            ops.set_launch_tuning(**tune)
+            assert torch.equal(ops.fp8blk_gemv(w, s, x), y0), tune
+            assert torch.equal(ops.fp8blk_gemv_argmax(w, s, x, ws), t0), tune
+    finally:
+        ops.set_launch_tuning()
+
+
 def test_tc_nan_code_only_poisons_its_row(ops):
     case = synth.fp8blk_case(300, 512, 3, seed=82)
     case.codes[133, 300] = 0x7F
