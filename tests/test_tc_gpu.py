@@ -165,6 +165,28 @@ def test_tc_bit_identical_under_launch_tuning(ops):
         ops.set_launch_tuning()
 
 
+def test_tc_replayed_from_a_cuda_graph(ops):
+    """The tensor-core GEMV recorded into a CUDA graph and replayed on new
+    activations gives the eager call's bits."""
+    rows, cols, m = 16384, 4096, 8
+    case = synth.fp8blk_case(rows, cols, m, seed=83)
+    w, s = to_dev(case.codes), scales_dev(case.scale_e8m0)
+    rng = np.random.default_rng(84)
+    xs = [to_dev(case.x)] + [to_dev(rng.standard_normal((m, cols), dtype=np.float32)) for _ in range(2)]
+    x_buf = xs[0].clone()
+    y = torch.empty((m, rows), dtype=torch.float32, device="cuda:0")
+    ops.fp8blk_gemv(w, s, x_buf, y=y)  # per-shape host state is set up outside the capture
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        ops.fp8blk_gemv(w, s, x_buf, y=y)
+    for x in xs:
+        x_buf.copy_(x)
+        g.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(y, ops.fp8blk_gemv(w, s, x))
+
+
 def test_tc_nan_code_only_poisons_its_row(ops):
     case = synth.fp8blk_case(300, 512, 3, seed=82)
     case.codes[133, 300] = 0x7F

@@ -81,3 +81,38 @@ def test_noalloc_refuses_shapes_beyond_its_array(ops):
     fake = ctypes.c_void_p(0x10000)  # never dereferenced: the size check comes first
     rc = lib.fp8blk_gemv_argmax_noalloc(fake, fake, fake, None, fake, 8, 100000, 8192, None)
     assert rc == ops.ERANGE
+
+
+@pytest.mark.parametrize("m,rows,cols", [(1, 131072, 4096), (8, 16384, 4096), (3, 1000, 1040)])
+def test_noalloc_inside_a_cuda_graph(ops, m, rows, cols):
+    """The call this entry point exists for: recorded once into a CUDA graph
+    (after one eager call on the device), then replayed with new activations
+    copied into the captured input buffer; each replay's tokens and logits
+    equal the workspace entry point's bit for bit."""
+    lib = ops.raw_library()
+    cases = [synth.fp8blk_case(rows, cols, m, seed=950 + k) for k in range(3)]
+    w, s = to_dev(cases[0].codes), scales_dev(cases[0].scale_e8m0)
+    xs = [to_dev(c.x) for c in cases]
+    x_buf = xs[0].clone()
+    tokens = torch.full((m,), -1, dtype=torch.int32, device="cuda:0")
+    logits = torch.empty((m, rows), dtype=torch.float32, device="cuda:0")
+
+    def call():
+        rc = lib.fp8blk_gemv_argmax_noalloc(
+            ctypes.c_void_p(w.data_ptr()), ctypes.c_void_p(s.data_ptr()), ctypes.c_void_p(x_buf.data_ptr()),
+            ctypes.c_void_p(logits.data_ptr()), ctypes.c_void_p(tokens.data_ptr()), m, rows, cols,
+            ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+        assert rc == ops.OK
+
+    call()  # the first call on the device precedes any capture (it looks up the array's address)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        call()
+    for x in xs:
+        x_buf.copy_(x)
+        g.replay()
+        torch.cuda.synchronize()
+        ref_tok, ref_logits = _reference(ops, w, s, x, m, rows, cols)
+        assert np.array_equal(tokens.cpu().numpy().view(np.uint32), ref_tok)
+        assert np.array_equal(logits.cpu().numpy().view(np.uint32), ref_logits.view(np.uint32))
