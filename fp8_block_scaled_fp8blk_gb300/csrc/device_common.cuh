@@ -120,21 +120,6 @@ __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
     asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
 
-// Named barrier `id` over `nthreads` threads that also ORs a per-thread flag:
-// every participant gets the same answer.
-__device__ __forceinline__ bool bar_sync_or(int id, int nthreads, bool flag) {
-    uint32_t r;
-    asm volatile(
-        "{\n\t.reg .pred q, p;\n\t"
-        "setp.ne.u32 q, %1, 0;\n\t"
-        "barrier.cta.red.or.pred p, %2, %3, q;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(r)
-        : "r"(static_cast<uint32_t>(flag)), "r"(id), "r"(nthreads)
-        : "memory");
-    return r != 0;
-}
-
 // ---------------------------------------------------------------- bulk copy
 // L2 policy for data read exactly once (weights): evict first.
 __device__ __forceinline__ uint64_t l2_policy_evict_first() {
