@@ -103,20 +103,21 @@ namespace {
 struct MapEntry {
     const void *ptr;
     int64_t rows, cols;
-    int box_rows, box_cols, dtype;
+    int box_rows, box_cols, dtype, swizzle;
     CUtensorMap map;
 };
 std::mutex g_map_mu;
 MapEntry g_maps[128];
 int g_map_next = 0;
 
-// Encodes (or finds) a 2-D tensor map of a rows x cols row-major array.
-cudaError_t tensor_map_2d(const void *ptr, int64_t rows, int64_t cols, int elem_bytes, CUtensorMapDataType dtype,
+// Encodes (or finds) a 2-D tensor map of a rows x cols row-major array whose
+// rows are row_bytes apart.
+cudaError_t tensor_map_2d(const void *ptr, int64_t rows, int64_t cols, int64_t row_bytes, CUtensorMapDataType dtype,
                           int box_rows, int box_cols, CUtensorMapSwizzle swizzle, CUtensorMap *out) {
     std::lock_guard<std::mutex> lock(g_map_mu);
     for (const MapEntry &e : g_maps)
         if (e.ptr == ptr && e.rows == rows && e.cols == cols && e.box_rows == box_rows && e.box_cols == box_cols &&
-            e.dtype == static_cast<int>(dtype)) {
+            e.dtype == static_cast<int>(dtype) && e.swizzle == static_cast<int>(swizzle)) {
             *out = e.map;
             return cudaSuccess;
         }
@@ -125,13 +126,13 @@ cudaError_t tensor_map_2d(const void *ptr, int64_t rows, int64_t cols, int elem_
     if (!fn) return err;
     CUtensorMap map;
     const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
-    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * elem_bytes};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(row_bytes)};
     const cuuint32_t box[2] = {static_cast<cuuint32_t>(box_cols), static_cast<cuuint32_t>(box_rows)};
     const cuuint32_t estr[2] = {1u, 1u};
     const CUresult r = fn(&map, dtype, 2, const_cast<void *>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                           swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
-    g_maps[g_map_next] = MapEntry{ptr, rows, cols, box_rows, box_cols, static_cast<int>(dtype), map};
+    g_maps[g_map_next] = MapEntry{ptr, rows, cols, box_rows, box_cols, static_cast<int>(dtype), static_cast<int>(swizzle), map};
     g_map_next = (g_map_next + 1) % 128;
     *out = map;
     return cudaSuccess;
@@ -139,8 +140,17 @@ cudaError_t tensor_map_2d(const void *ptr, int64_t rows, int64_t cols, int elem_
 }  // namespace
 
 cudaError_t weight_tensor_map(const uint8_t *w, int64_t rows, int64_t cols, int box_rows, CUtensorMap *out) {
-    return tensor_map_2d(w, rows, cols, 1, CU_TENSOR_MAP_DATA_TYPE_UINT8, box_rows, kT8Kb, CU_TENSOR_MAP_SWIZZLE_128B,
+    return tensor_map_2d(w, rows, cols, cols, CU_TENSOR_MAP_DATA_TYPE_UINT8, box_rows, kT8Kb, CU_TENSOR_MAP_SWIZZLE_128B,
                          out);
+}
+
+cudaError_t nvfp4_tensor_maps(const uint8_t *codes, const uint8_t *scales, int64_t total_rows, int64_t cols,
+                              int box_rows, CUtensorMap *cmap, CUtensorMap *smap) {
+    const cudaError_t err = tensor_map_2d(codes, total_rows, cols, cols / 2, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B,
+                                          box_rows, 128, CU_TENSOR_MAP_SWIZZLE_128B, cmap);
+    if (err != cudaSuccess) return err;
+    return tensor_map_2d(scales, total_rows, cols / 16, cols / 16, CU_TENSOR_MAP_DATA_TYPE_UINT8, box_rows,
+                         kF4StageColsHost / 16, CU_TENSOR_MAP_SWIZZLE_NONE, smap);
 }
 
 static int pow2_floor(int v) {
@@ -563,6 +573,12 @@ int fp8blk_set_tensor_core_min_m(int min_m, int64_t min_bytes) {
     if (min_bytes < 0) return FP8BLK_EINVAL;
     tuning().tc_min_m = min_m == 0 ? Tuning().tc_min_m : min_m;
     tuning().tc_min_bytes = min_bytes == 0 ? Tuning().tc_min_bytes : min_bytes;
+    return FP8BLK_OK;
+}
+
+int fp8blk_set_fp4_kernel(int choice) {
+    if (choice < 0 || choice > 2) return FP8BLK_EINVAL;
+    tuning().fp4_kernel = choice;
     return FP8BLK_OK;
 }
 

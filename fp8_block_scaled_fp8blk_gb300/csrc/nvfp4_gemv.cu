@@ -1,13 +1,76 @@
 // nvfp4_gemv.cu -- plan and launch of the one-launch FP4 (NVFP4 / MXFP4)
 // routed-expert GEMV (nvfp4_gemv.cuh).
 #include "launch.h"
+#include "fp4tc_gemv.cuh"
 #include "nvfp4_gemv.cuh"
 
 namespace fp8blk {
 
 constexpr int kNvStageTarget = 16384;  // bytes of two stages (R rows each) the row count aims at
 
+// Rows per unit for the tensor-core FP4 kernel: the smallest multiple of 8
+// (at most 128) whose units, n_active x ceil(rows / R), fit one per SM.
+static int f4_slab_rows(const Nvfp4Args &a, const DeviceInfo &dev) {
+    for (int r = 8; r < 128; r += 8)
+        if (static_cast<int64_t>(a.n_active) * ((a.rows + r - 1) / r) <= dev.sms) return r;
+    return 128;
+}
+
+// NVFP4 on the tensor cores: one CTA per SM over contiguous ranges of
+// (slot, slab) units.
+static cudaError_t launch_fp4tc(const Nvfp4Args &a, const DeviceInfo &dev, cudaStream_t stream) {
+    F4Args f = {};
+    f.nv = a;
+    f.slab_rows = f4_slab_rows(a, dev);
+    f.raw_stages = f4_raw_stages(a.cols, f.slab_rows, dev.smem_per_block - kStaticSmemReserve);
+    if (f.raw_stages < kF4MinRawStages) return cudaErrorInvalidConfiguration;
+    f.n_slabs = (a.rows + f.slab_rows - 1) / f.slab_rows;
+    f.units = f.n_slabs * a.n_active;
+    CUtensorMap cmap, smap;
+    cudaError_t err = nvfp4_tensor_maps(a.codes, a.scales, static_cast<int64_t>(a.n_experts) * a.rows, a.cols,
+                                        f.slab_rows, &cmap, &smap);
+    if (err != cudaSuccess) return err;
+    const size_t smem = f4_smem_bytes(a.cols, f.raw_stages, f.slab_rows);
+    int per_sm = 0;
+    err = kernel_occupancy(reinterpret_cast<const void *>(fp4tc_gemv_kernel), kF4Threads, smem, &per_sm);
+    if (err != cudaSuccess) return err;
+    if (per_sm < 1) return cudaErrorInvalidConfiguration;
+    int64_t grid = dev.sms;
+    if (grid > f.units) grid = f.units;
+    if (grid > kMaxGrid) grid = kMaxGrid;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(grid));
+    cfg.blockDim = dim3(kF4Threads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = tuning().use_pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, fp4tc_gemv_kernel, cmap, smap, f);
+}
+
+// By shape, NVFP4 experts take the tensor cores from this many active rows
+// (n_active x rows) on: below it the slabs are too short for the per-stage
+// copies to reach the CUDA-core kernel's rate (6 x 2048 rows: 12.7 vs 12.5
+// us; 12 x 2048: 20.2 vs 21.5 us; 64 x 2048: 60.3 vs 86.3 us).
+constexpr int64_t kF4TcMinActiveRows = 16384;
+
+// NVFP4 experts take the tensor cores when chosen (by shape or pinned) and
+// the codes start on a 32-byte boundary (the packed-code TMA type), the slab
+// rows fit 32-bit TMA coordinates over the experts' stacked rows, and B plus
+// a minimal ring fit in shared memory.
+static bool fp4_use_tensor_cores(const Nvfp4Args &a, const DeviceInfo &dev) {
+    if (tuning().fp4_kernel == 1) return false;
+    if (tuning().fp4_kernel == 0 && static_cast<int64_t>(a.n_active) * a.rows < kF4TcMinActiveRows) return false;
+    return (reinterpret_cast<uintptr_t>(a.codes) & 31u) == 0 &&
+           static_cast<int64_t>(a.n_experts) * a.rows + 128 <= (1ll << 31) - 1 &&
+           f4_raw_stages(a.cols, f4_slab_rows(a, dev), dev.smem_per_block - kStaticSmemReserve) >= kF4MinRawStages;
+}
+
 cudaError_t launch_fp4_expert_gemv(Nvfp4Args a, bool mxfp4, const DeviceInfo &dev, cudaStream_t stream) {
+    if (!mxfp4 && fp4_use_tensor_cores(a, dev)) return launch_fp4tc(a, dev, stream);
     a.panels = static_cast<int>((a.cols + kNvMaxPanel - 1) / kNvMaxPanel);
     a.panel_cols = a.panels == 1 ? static_cast<int>(a.cols) : kNvMaxPanel;
     const int row_bytes = a.panel_cols / 2 + a.panel_cols / (mxfp4 ? 32 : 16);

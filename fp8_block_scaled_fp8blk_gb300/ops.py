@@ -58,6 +58,8 @@ _lib.fp8blk_set_launch_tuning.restype = _INT
 _lib.fp8blk_set_launch_tuning.argtypes = [_INT, _INT, _INT, _INT, _INT]
 _lib.fp8blk_set_m1_kernel.restype = _INT
 _lib.fp8blk_set_m1_kernel.argtypes = [_INT, _I64]
+_lib.fp8blk_set_fp4_kernel.restype = _INT
+_lib.fp8blk_set_fp4_kernel.argtypes = [_INT]
 _lib.fp8blk_set_wait_limit.restype = _INT
 _lib.fp8blk_set_wait_limit.argtypes = [_I64]
 _lib.fp8blk_set_tensor_core_min_m.restype = _INT
@@ -289,6 +291,11 @@ def plan_query(m: int, rows: int, cols: int, bytes_per_weight: int = 1, sms: int
 def set_m1_kernel(choice: int = 0, rowwarp_min_bytes: int = 0) -> None:
     """m = 1 kernel: 0 by size, 1 row-per-warp, 2 team (speed only)."""
     _check(_lib.fp8blk_set_m1_kernel(choice, rowwarp_min_bytes), "fp8blk_set_m1_kernel")
+
+
+def set_fp4_kernel(choice: int = 0) -> None:
+    """NVFP4 expert GEMV kernel: 0 by shape, 1 CUDA cores, 2 tensor cores (speed only)."""
+    _check(_lib.fp8blk_set_fp4_kernel(choice), "fp8blk_set_fp4_kernel")
 
 
 def set_tensor_core_min_m(min_m: int = 0, min_bytes: int = 0) -> None:

@@ -311,6 +311,22 @@ int fp8blk_set_wait_limit(int64_t limit_ns);
 int fp8blk_set_m1_kernel(int choice, int64_t rowwarp_min_bytes);
 
 /*
+ * fp8blk_set_fp4_kernel -- which kernel serves nvfp4_expert_gemv (speed only;
+ * both are within the stated error bound, each bit-identical run to run):
+ *   0 = by shape: the tensor cores from 16384 active rows (n_active x rows)
+ *   on, the CUDA cores below; 1 = CUDA cores (weights decoded to f32 in
+ *   registers, one f32 FMA each); 2 = tensor cores (the e2m1 codes fed to
+ *   tcgen05.mma kind::f8f6f4 as stored, x as five e4m3 planes per 16-column
+ *   block, the block scales applied to the f32 block sums).  The tensor
+ *   cores also need 32-byte-aligned codes and room in shared memory for x's
+ *   planes (16 bytes per column) beside three stages (cols up to 6656 with
+ *   128-row slabs), else the CUDA cores serve the call; with an inf or NaN in
+ *   x they return NaN in every output, the CUDA cores the IEEE result.
+ *   mxfp4_expert_gemv always runs on the CUDA cores.  Errors: EINVAL.
+ */
+int fp8blk_set_fp4_kernel(int choice);
+
+/*
  * fp8blk_set_tensor_core_min_m -- route e4m3 GEMVs with m >= min_m activation
  * rows (1..8; 9 = never; 0 = the library default, 1) and at least min_bytes
  * of weights (rows * cols; 1 = any size; 0 = the library default, which

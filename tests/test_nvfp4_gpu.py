@@ -73,18 +73,30 @@ def test_expert_dequant_gemv_ragged(ops):
     assert_close(y, ref, a, "nvfp4 ragged")
 
 
-# ---- one-launch expert GEMV, NVFP4 decoded in registers, ids on the device
+# ---- one-launch expert GEMV, ids on the device: NVFP4 decoded in registers
+# (CUDA cores) or into exact f16 tiles for kind::f16 MMAs (tensor cores)
 
-def fused(ops, case, ids=None, gscale=None):
+@pytest.fixture(params=[1, 2], ids=["cuda_cores", "tensor_cores"])
+def fp4k(ops, request):
+    ops.set_fp4_kernel(request.param)
+    yield request.param
+    ops.set_fp4_kernel(0)
+
+def fused(ops, case, ids=None, gscale=None, status=0):
+    """One call into a NaN-filled output; the device status word must then
+    read `status` (a kernel that gave up would leave NaNs and set bit 0)."""
     ids = case.ids if ids is None else ids
     g = case.gscale if gscale is None else gscale
-    y = ops.nvfp4_expert_gemv(to_dev(case.codes), to_dev(case.scales), to_dev(np.asarray(g, dtype=np.float32)),
-                              to_dev(np.asarray(ids, dtype=np.int32)), to_dev(case.x))
+    y = torch.full((len(ids), case.codes.shape[1]), float("nan"), dtype=torch.float32, device="cuda:0")
+    ops.nvfp4_expert_gemv(to_dev(case.codes), to_dev(case.scales), to_dev(np.asarray(g, dtype=np.float32)),
+                          to_dev(np.asarray(ids, dtype=np.int32)), to_dev(case.x), y=y)
     torch.cuda.synchronize()
+    got = ops.fp8blk_device_status(clear=True)
+    assert got == status, f"device status {got:#x}, expected {status:#x}"
     return y.cpu().numpy()
 
 
-def test_fused_expert_gemv_full_config(ops, c5):
+def test_fused_expert_gemv_full_config(ops, fp4k, c5):
     y = fused(ops, c5)
     ref, a, _ = oracle.nvfp4_expert_dequant_gemv(c5.codes, c5.scales, c5.gscale, c5.ids, c5.x, nthreads=16)
     assert_close(y, ref, a, "fused nvfp4 C5")
@@ -92,17 +104,19 @@ def test_fused_expert_gemv_full_config(ops, c5):
 
 @pytest.mark.parametrize("n_experts,rows,cols,n_active", [(3, 1, 256, 1), (4, 7, 512, 2), (8, 129, 4096, 3),
                                                           (5, 1000, 1280, 5), (6, 130, 4352, 4),
-                                                          (4, 65, 8192, 4), (70, 64, 256, 70)])
-def test_fused_expert_gemv_ragged(ops, n_experts, rows, cols, n_active):
+                                                          (4, 65, 8192, 4), (70, 64, 256, 70),
+                                                          (64, 300, 512, 64)])
+def test_fused_expert_gemv_ragged(ops, fp4k, n_experts, rows, cols, n_active):
     """Ragged rows, one and several column panels (4352 = 4096 + 256), every
-    expert active, more slots than one row group each."""
+    expert active, more slots than one row group each, and more (slot, slab)
+    units than SMs (64 x 300 rows)."""
     case = synth.nvfp4_case(n_experts, rows, cols, n_active, seed=rows * 31 + cols + n_active)
     y = fused(ops, case)
     ref, a, _ = oracle.nvfp4_expert_dequant_gemv(case.codes, case.scales, case.gscale, case.ids, case.x, nthreads=8)
     assert_close(y, ref, a, f"fused nvfp4 {n_experts}x{rows}x{cols} k={n_active}")
 
 
-def test_fused_expert_gemv_repeated_ids_and_scales(ops):
+def test_fused_expert_gemv_repeated_ids_and_scales(ops, fp4k):
     """Repeated ids are allowed on the device path; per-expert global scales
     other than 2^-4 (any power of two) scale the result exactly."""
     case = synth.nvfp4_case(4, 300, 1024, 3, seed=55)
@@ -114,19 +128,19 @@ def test_fused_expert_gemv_repeated_ids_and_scales(ops):
     assert_close(y[:2], ref, a, "fused nvfp4 scales")
 
 
-def test_fused_expert_gemv_bad_expert_is_nan_and_flagged(ops):
+def test_fused_expert_gemv_bad_expert_is_nan_and_flagged(ops, fp4k):
     case = synth.nvfp4_case(4, 200, 512, 3, seed=56)
     assert ops.fp8blk_device_status(clear=True) == 0
     g = np.array([2.0 ** -4, 0.75, 2.0 ** -4, 2.0 ** -4], dtype=np.float32)  # expert 1: not a power of two
-    y = fused(ops, case, ids=np.array([3, 9, 1], dtype=np.int32), gscale=g)  # 9: out of range
+    y = fused(ops, case, ids=np.array([3, 9, 1], dtype=np.int32), gscale=g,  # 9: out of range
+              status=ops.STATUS_BAD_EXPERT)
     assert np.isnan(y[1]).all() and np.isnan(y[2]).all()
     ref, a, _ = oracle.nvfp4_expert_dequant_gemv(case.codes, case.scales, g, np.array([3], dtype=np.int32), case.x)
     assert_close(y[:1], ref, a, "good slot next to bad ones")
-    assert ops.fp8blk_device_status(clear=True) == ops.STATUS_BAD_EXPERT
     assert ops.fp8blk_device_status() == 0
 
 
-def test_fused_matches_two_step_path(ops, c5):
+def test_fused_matches_two_step_path(ops, fp4k, c5):
     """Both arms use the same bf16 weight values; their sums agree within the
     GEMV tolerance of each other."""
     codes, scales, x = to_dev(c5.codes), to_dev(c5.scales), to_dev(c5.x)
@@ -138,8 +152,10 @@ def test_fused_matches_two_step_path(ops, c5):
     assert np.all(np.abs(y1.astype(np.float64) - y2) <= 2 * (1e-5 * a + 1e-6))
 
 
-def test_fused_x_wide_dynamic_range(ops):
-    """x spanning 2^-40 .. 2^20: the f32 sums keep the small terms' share."""
+def test_fused_x_wide_dynamic_range(ops, fp4k):
+    """x spanning 2^-40 .. 2^20: the f32 sums keep the small terms' share (the
+    tensor-core arm's f16 planes are scaled by max|x|; small entries sit far
+    below it)."""
     case = synth.nvfp4_case(3, 256, 2048, 2, seed=77)
     rng = np.random.default_rng(78)
     x = (rng.standard_normal(2048) * np.exp2(rng.integers(-40, 21, 2048))).astype(np.float32)
@@ -149,7 +165,7 @@ def test_fused_x_wide_dynamic_range(ops):
     assert_close(y, ref, a, "fused nvfp4 wide x")
 
 
-def test_fused_nan_scale_poisons_only_its_row(ops):
+def test_fused_nan_scale_poisons_only_its_row(ops, fp4k):
     """An e4m3 NaN scale (0x7F) makes its 16 weights NaN: that row's output is
     NaN, every other row is untouched."""
     case = synth.nvfp4_case(2, 300, 1024, 2, seed=79)
@@ -165,7 +181,58 @@ def test_fused_nan_scale_poisons_only_its_row(ops):
     assert_close(y[ok], ref[ok], a[ok], "rows next to the NaN scale")
 
 
-def test_fused_bit_identical_rerun(ops, c5):
+def test_fused_bit_identical_rerun(ops, fp4k, c5):
     """Two calls on the same inputs give the same bits (fixed reduction order)."""
     y1, y2 = fused(ops, c5), fused(ops, c5)
     assert np.array_equal(y1.view(np.uint32), y2.view(np.uint32))
+
+
+def test_fused_x_inf_and_nan(ops, fp4k):
+    """An inf in x (next to a large finite element): the CUDA-core arm gives
+    +-inf where its weight is nonzero and NaN where it is zero (0 * inf), as
+    the oracle does; the tensor-core arm gives NaN everywhere (every exact sum
+    is non-finite).  A NaN in x makes every output NaN on both."""
+    case = synth.nvfp4_case(2, 256, 1024, 2, seed=81)
+    x = case.x.copy()
+    x[100] = np.inf
+    x[700] = 1e30
+    cx = synth.Nvfp4Case(case.codes, case.scales, case.gscale, case.ids, x)
+    y = fused(ops, cx)
+    ref, _, _ = oracle.nvfp4_expert_dequant_gemv(cx.codes, cx.scales, cx.gscale, cx.ids, cx.x, nthreads=8)
+    assert np.isnan(ref).any() and np.isinf(ref).any() and not np.isfinite(ref).any()
+    if fp4k == 1:
+        assert np.array_equal(np.isnan(y), np.isnan(ref))
+        assert np.array_equal(y[~np.isnan(ref)], ref[~np.isnan(ref)])
+    else:  # e4m3 planes hold no inf: the non-finite block poisons every sum
+        assert np.isnan(y).all()
+    x[5] = np.nan
+    y = fused(ops, synth.Nvfp4Case(case.codes, case.scales, case.gscale, case.ids, x))
+    assert np.isnan(y).all()
+
+
+def test_fused_kernels_agree(ops, c5):
+    """Both arms within the GEMV tolerance of each other on the full workload."""
+    runs = {}
+    for k in (1, 2):
+        ops.set_fp4_kernel(k)
+        runs[k] = fused(ops, c5)
+    ops.set_fp4_kernel(0)
+    _, a, _ = oracle.nvfp4_expert_dequant_gemv(c5.codes, c5.scales, c5.gscale, c5.ids, c5.x, nthreads=16)
+    assert np.all(np.abs(runs[1].astype(np.float64) - runs[2]) <= 2 * (1e-5 * a + 1e-6))
+
+
+def test_fused_default_routes_by_shape(ops):
+    """The by-shape default gives the CUDA-core kernel's bits below 16384
+    active rows and the tensor-core kernel's bits from there on."""
+    small = synth.nvfp4_case(8, 256, 1024, 2, seed=83)          # 512 active rows
+    large = synth.nvfp4_case(16, 2048, 512, 16, seed=84)        # 32768 active rows
+    for case, arm in ((small, 1), (large, 2)):
+        ops.set_fp4_kernel(0)
+        y0 = fused(ops, case)
+        ops.set_fp4_kernel(arm)
+        y1 = fused(ops, case)
+        ops.set_fp4_kernel(0)
+        assert np.array_equal(y0.view(np.uint32), y1.view(np.uint32)), f"default is not arm {arm}"
+    ref, a, _ = oracle.nvfp4_expert_dequant_gemv(large.codes, large.scales, large.gscale, large.ids, large.x,
+                                                 nthreads=16)
+    assert_close(y0, ref, a, "fused nvfp4 16 x 2048 x 512, tensor cores")
