@@ -84,8 +84,8 @@ def nvfp4_bytes(n_active: int, rows: int, cols: int) -> int:
 
 # Sources that define the streaming kernels and their launch geometry.
 KERNEL_SOURCES = ("device_common.cuh", "stream_gemv.cuh", "rowwarp_gemv.cuh", "tc8_gemv.cuh", "nvfp4_gemv.cuh",
-                  "launch.h", "abi.cu", "gemv_e4m3.cu", "gemv_bf16.cu", "gemv_tc.cu", "nvfp4_dequant.cu",
-                  "nvfp4_gemv.cu")
+                  "fp4tc_gemv.cuh", "launch.h", "abi.cu", "gemv_e4m3.cu", "gemv_bf16.cu", "gemv_tc.cu",
+                  "nvfp4_dequant.cu", "nvfp4_gemv.cu")
 
 
 # The sources that decide each profiled workload's dominant kernel and its
@@ -95,8 +95,12 @@ TRAFFIC_SOURCES = {
     "head_argmax_131072x4096_m1": _PLAN_SOURCES + ("stream_gemv.cuh", "tc8_gemv.cuh", "gemv_tc.cu"),
     "verify_16384x4096_m8": _PLAN_SOURCES + ("stream_gemv.cuh", "tc8_gemv.cuh", "gemv_tc.cu"),
     "gemv_4096x4096_m1": _PLAN_SOURCES + ("stream_gemv.cuh", "gemv_e4m3.cu"),
-    "nvfp4_experts_6of64_2048x4096": _PLAN_SOURCES + ("rowwarp_gemv.cuh", "nvfp4_gemv.cuh", "nvfp4_gemv.cu"),
-    "mxfp4_experts_6of64_2048x4096": _PLAN_SOURCES + ("rowwarp_gemv.cuh", "nvfp4_gemv.cuh", "nvfp4_gemv.cu"),
+    "nvfp4_experts_6of64_2048x4096": _PLAN_SOURCES + ("rowwarp_gemv.cuh", "nvfp4_gemv.cuh", "fp4tc_gemv.cuh",
+                                                      "nvfp4_gemv.cu"),
+    "nvfp4_experts_64of64_2048x4096": _PLAN_SOURCES + ("tc8_gemv.cuh", "nvfp4_gemv.cuh", "fp4tc_gemv.cuh",
+                                                       "nvfp4_gemv.cu"),
+    "mxfp4_experts_6of64_2048x4096": _PLAN_SOURCES + ("rowwarp_gemv.cuh", "nvfp4_gemv.cuh", "fp4tc_gemv.cuh",
+                                                      "nvfp4_gemv.cu"),
 }
 
 
@@ -332,11 +336,12 @@ def setup_fp8blk(name: str, device, argmax: bool = False):
                 x=x, workspaces=wsp, argmax=argmax, launches=1, bytes=fp8blk_bytes(rows, cols, m, argmax))
 
 
-def setup_nvfp4(device, fused: bool = True):
+def setup_nvfp4(device, fused: bool = True, n_active: int | None = None):
     """C5 with ten rotating active-expert sets (the 64-expert pool is 301 MB, so
     the active experts' bytes come from HBM).  fused: one launch per call
-    (in-register decode, ids and global scales on the device); otherwise the
-    dequant-to-scratch + bf16 GEMV arm, two launches per active expert."""
+    (ids and global scales on the device); otherwise the dequant-to-scratch +
+    bf16 GEMV arm, two launches per active expert.  n_active: another number
+    of active experts drawn from the same pool (default: C5's six)."""
     import numpy as np
     import torch
     from fp8_block_scaled_fp8blk_gb300 import ops, synth
@@ -344,10 +349,11 @@ def setup_nvfp4(device, fused: bool = True):
     c = synth.nvfp4_case(w["n_experts"], w["rows"], w["cols"], w["n_active"], w["seed"])
     codes, scales, x = up(c.codes, device), up(c.scales, device), up(c.x, device)
     rows, cols = w["rows"], w["cols"]
+    act = w["n_active"] if n_active is None else n_active
     rng = np.random.default_rng(w["seed"] + 100)
-    id_sets = [c.ids] + [rng.choice(w["n_experts"], w["n_active"], replace=False).astype(np.int32)
-                         for _ in range(9)]
-    ys = [torch.empty((w["n_active"], rows), dtype=torch.float32, device=device) for _ in id_sets]
+    id_sets = ([c.ids] if act == w["n_active"] else []) + [
+        rng.choice(w["n_experts"], act, replace=False).astype(np.int32) for _ in range(9 if act == w["n_active"] else 10)]
+    ys = [torch.empty((act, rows), dtype=torch.float32, device=device) for _ in id_sets]
     if fused:
         g_dev = up(c.gscale, device)
         ids_dev = [up(np.asarray(i, dtype=np.int32), device) for i in id_sets]
@@ -358,8 +364,8 @@ def setup_nvfp4(device, fused: bool = True):
         scratch = torch.empty((rows, cols), dtype=torch.int16, device=device)
         calls = [lambda i=i: ops.nvfp4_expert_dequant_gemv(codes, scales, c.gscale, id_sets[i], x,
                                                            scratch, y=ys[i]) for i in range(len(id_sets))]
-        launches = 2 * w["n_active"]
-    return dict(calls=calls, bytes=nvfp4_bytes(w["n_active"], rows, cols), launches=launches)
+        launches = 2 * act
+    return dict(calls=calls, bytes=nvfp4_bytes(act, rows, cols), launches=launches)
 
 
 def mxfp4_bytes(n_active: int, rows: int, cols: int) -> int:
@@ -441,13 +447,30 @@ def measure_extra(device, stream, world, peak, steps, warmup, sampler):
     del st
     for fused, name, note in (
             (True, "nvfp4_experts_6of64_2048x4096",
-             "one launch: NVFP4 decoded in registers, expert ids and global scales on the device"),
+             "one launch, the by-shape default (CUDA cores here): NVFP4 decoded in registers, expert ids "
+             "and global scales on the device"),
             (False, "nvfp4_experts_6of64_2048x4096_two_step",
              "dequant to the reused bf16 scratch + bf16 GEMV per expert; algorithmic bytes exclude "
              "the 2 x 16 MiB scratch write+read per expert")):
         st = setup_nvfp4(device, fused)
         r = time_reps(st["calls"], steps, warmup, stream, world, device)
         out[name] = summarize(st, r, steps, peak, sampler, note=note)
+        del st
+    # The one-launch NVFP4 GEMV on both kernels, with C5's six and with all 64
+    # experts active (the tensor-core kernel is the by-shape default from
+    # 16384 active rows on).
+    for act, name in ((6, "nvfp4_experts_6of64_2048x4096"), (64, "nvfp4_experts_64of64_2048x4096")):
+        st = setup_nvfp4(device, True, act)
+        for k, arm in ((2, "_tensor_core"), (1, "_cuda_core")):
+            if act == 6 and k == 1:
+                continue  # the default line above
+            ops.set_fp4_kernel(k)
+            r = time_reps(st["calls"], steps, warmup, stream, world, device)
+            out[name + arm] = summarize(
+                st, r, steps, peak, sampler,
+                note="one launch on the tensor cores: e2m1 codes fed to tcgen05 kind::f8f6f4 as stored"
+                if k == 2 else "one launch on the CUDA cores: NVFP4 decoded in registers")
+        ops.set_fp4_kernel(0)
         del st
     st = setup_mxfp4(device)
     r = time_reps(st["calls"], steps, warmup, stream, world, device)
@@ -718,6 +741,8 @@ def run_profile_workload(args):
         st = setup_mxfp4(device)
     elif args.profile_workload.startswith("nvfp4_experts_6of64_2048x4096"):
         st = setup_nvfp4(device, fused=not args.profile_workload.endswith("_two_step"))
+    elif args.profile_workload == "nvfp4_experts_64of64_2048x4096":
+        st = setup_nvfp4(device, True, 64)
     else:
         st = setup_fp8blk(args.profile_workload, device, args.profile_workload.startswith("head_argmax"))
     for i in range(args.calls):
