@@ -237,8 +237,9 @@ def nvfp4_expert_dequant_gemv(codes: torch.Tensor, scales: torch.Tensor, gscale,
 
 def nvfp4_expert_gemv(codes: torch.Tensor, scales: torch.Tensor, gscale: torch.Tensor, ids: torch.Tensor,
                       x: torch.Tensor, y: torch.Tensor | None = None) -> torch.Tensor:
-    """y [n_active, rows] = W(ids[k]) x in one launch, NVFP4 decoded in registers;
-    `gscale` (f32 [n_experts]) and `ids` (int32 [n_active]) stay on the device."""
+    """y [n_active, rows] = W(ids[k]) x in one launch (CUDA cores or tensor
+    cores, see set_fp4_kernel); `gscale` (f32 [n_experts]) and `ids` (int32
+    [n_active]) stay on the device."""
     n_experts, rows, half = codes.shape
     cols = 2 * half
     if gscale.dtype != torch.float32 or ids.dtype != torch.int32:
@@ -294,7 +295,8 @@ def set_m1_kernel(choice: int = 0, rowwarp_min_bytes: int = 0) -> None:
 
 
 def set_fp4_kernel(choice: int = 0) -> None:
-    """NVFP4 expert GEMV kernel: 0 by shape, 1 CUDA cores, 2 tensor cores (speed only)."""
+    """NVFP4 expert GEMV kernel: 0 by shape (tensor cores from 16384 active
+    rows on), 1 CUDA cores, 2 tensor cores."""
     _check(_lib.fp8blk_set_fp4_kernel(choice), "fp8blk_set_fp4_kernel")
 
 

@@ -218,10 +218,15 @@ int nvfp4_expert_dequant_gemv(const uint8_t *codes, const uint8_t *scales,
 
 /*
  * nvfp4_expert_gemv -- y[k] = W(ids[k]) x for k < n_active in ONE launch,
- * decoding the NVFP4 weights in registers (no bf16 scratch):
+ * with no bf16 scratch:
  *   y[k][r] = sum_c bf16(e2m1(q[e][r][c]) * e4m3(s[e][r][c/16]) * g[e]) * x[c],
  *   e = ids[k]; every product is exact, so the weights take the same values
- *   as nvfp4_expert_dequant writes; the sum is in f32.
+ *   as nvfp4_expert_dequant writes; the sum is in f32.  Two kernels
+ *   (fp8blk_set_fp4_kernel; by shape, the tensor cores from 16384 active rows
+ *   on): the CUDA cores decode the weights in registers; the tensor cores take
+ *   the codes as stored, x as five e4m3 planes per 16-column block (2^-20 of
+ *   each element), and apply the block scales to the f32 block sums.  Both
+ *   meet the GEMV error bound and are bit-identical run to run.
  * Source: "Module dsv4_gpu" page, module header (routed experts stay NVFP4 as
  * stored; one-launch-per-projection indirect expert dispatch) and enum
  * ExpertArm.  The router's output stays on the device: ids and global scales
@@ -236,6 +241,8 @@ int nvfp4_expert_dequant_gemv(const uint8_t *codes, const uint8_t *scales,
  *   cols         a multiple of 256 (so every scale row starts on 16 bytes).
  * An id outside [0, n_experts) or an unusable global scale sets
  * FP8BLK_STATUS_BAD_EXPERT in the device status word and makes y[k] NaN.
+ * An inf or NaN in x: the CUDA cores give the IEEE result, the tensor cores
+ * NaN in every output.
  * Errors: EINVAL, EALIGN, ERANGE, ECUDA.
  */
 int nvfp4_expert_gemv(const uint8_t *codes, const uint8_t *scales, const float *gscale, int n_experts,
