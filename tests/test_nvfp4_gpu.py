@@ -236,3 +236,60 @@ def test_fused_default_routes_by_shape(ops):
     ref, a, _ = oracle.nvfp4_expert_dequant_gemv(large.codes, large.scales, large.gscale, large.ids, large.x,
                                                  nthreads=16)
     assert_close(y0, ref, a, "fused nvfp4 16 x 2048 x 512, tensor cores")
+
+
+def test_fused_tensor_cores_replayed_from_a_cuda_graph(ops):
+    """The tensor-core expert GEMV recorded into a CUDA graph and replayed on
+    new activations and new device ids gives the eager call's bits."""
+    case = synth.nvfp4_case(16, 2048, 1024, 8, seed=85)
+    codes, scales, g = to_dev(case.codes), to_dev(case.scales), to_dev(np.asarray(case.gscale, dtype=np.float32))
+    rng = np.random.default_rng(86)
+    ids_l = [np.asarray(case.ids, dtype=np.int32)] + [rng.choice(16, 8, replace=False).astype(np.int32)
+                                                       for _ in range(2)]
+    xs = [to_dev(case.x)] + [to_dev(rng.standard_normal(1024, dtype=np.float32)) for _ in range(2)]
+    ids_buf, x_buf = to_dev(ids_l[0]).clone(), xs[0].clone()
+    y = torch.empty((8, 2048), dtype=torch.float32, device="cuda:0")
+    ops.set_fp4_kernel(2)
+    try:
+        ops.nvfp4_expert_gemv(codes, scales, g, ids_buf, x_buf, y=y)  # per-shape host state outside the capture
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            ops.nvfp4_expert_gemv(codes, scales, g, ids_buf, x_buf, y=y)
+        for ids, x in zip(ids_l, xs):
+            ids_buf.copy_(to_dev(ids))
+            x_buf.copy_(x)
+            graph.replay()
+            torch.cuda.synchronize()
+            assert torch.equal(y, ops.nvfp4_expert_gemv(codes, scales, g, to_dev(ids), x))
+    finally:
+        ops.set_fp4_kernel(0)
+    assert ops.fp8blk_device_status(clear=True) == 0
+
+
+def test_tensor_core_kernels_back_to_back(ops):
+    """The NVFP4 and e4m3 tensor-core kernels (each holding all of an SM's
+    tensor memory) queued back to back on one stream, with programmatic
+    dependent launch, give the bits of the same calls made one at a time."""
+    c4 = synth.nvfp4_case(8, 1024, 2048, 8, seed=87)
+    f = synth.fp8blk_case(16384, 4096, 8, seed=88)
+    codes, scales, g, ids, x4 = (to_dev(c4.codes), to_dev(c4.scales),
+                                 to_dev(np.asarray(c4.gscale, dtype=np.float32)),
+                                 to_dev(np.asarray(c4.ids, dtype=np.int32)), to_dev(c4.x))
+    w, s, x8 = to_dev(f.codes), to_dev(ops.fp8blk_scales_from_e8m0(f.scale_e8m0)), to_dev(f.x)
+    ops.set_fp4_kernel(2)
+    try:
+        ref4 = ops.nvfp4_expert_gemv(codes, scales, g, ids, x4)
+        torch.cuda.synchronize()
+        ref8 = ops.fp8blk_gemv(w, s, x8)
+        torch.cuda.synchronize()
+        outs = []
+        for _ in range(3):
+            outs.append(ops.nvfp4_expert_gemv(codes, scales, g, ids, x4))
+            outs.append(ops.fp8blk_gemv(w, s, x8))
+        torch.cuda.synchronize()
+        for k, o in enumerate(outs):
+            assert torch.equal(o, ref4 if k % 2 == 0 else ref8), k
+    finally:
+        ops.set_fp4_kernel(0)
+    assert ops.fp8blk_device_status(clear=True) == 0
