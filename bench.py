@@ -101,6 +101,8 @@ TRAFFIC_SOURCES = {
                                                        "nvfp4_gemv.cu"),
     "mxfp4_experts_6of64_2048x4096": _PLAN_SOURCES + ("rowwarp_gemv.cuh", "nvfp4_gemv.cuh", "fp4tc_gemv.cuh",
                                                       "nvfp4_gemv.cu"),
+    "mxfp4_experts_64of64_2048x4096": _PLAN_SOURCES + ("tc8_gemv.cuh", "nvfp4_gemv.cuh", "fp4tc_gemv.cuh",
+                                                       "nvfp4_gemv.cu"),
 }
 
 
@@ -374,21 +376,23 @@ def mxfp4_bytes(n_active: int, rows: int, cols: int) -> int:
     return n_active * (rows * cols // 2 + rows * cols // 32) + 4 * cols + 4 * n_active * rows
 
 
-def setup_mxfp4(device):
-    """The MTP block's OCP MXFP4 experts, C5 geometry, ten rotating active sets."""
+def setup_mxfp4(device, n_active: int | None = None):
+    """The MTP block's OCP MXFP4 experts, C5 geometry, ten rotating active sets
+    (of C5's six experts, or of `n_active`)."""
     import numpy as np
     import torch
     from fp8_block_scaled_fp8blk_gb300 import ops, synth
     w = synth.MXFP4_WORKLOAD
     c = synth.mxfp4_case(w["n_experts"], w["rows"], w["cols"], w["n_active"], w["seed"])
     codes, scales, x = up(c.codes, device), up(c.scales, device), up(c.x, device)
+    act = w["n_active"] if n_active is None else n_active
     rng = np.random.default_rng(w["seed"] + 100)
-    id_sets = [c.ids] + [rng.choice(w["n_experts"], w["n_active"], replace=False).astype(np.int32)
-                         for _ in range(9)]
+    id_sets = ([c.ids] if act == w["n_active"] else []) + [
+        rng.choice(w["n_experts"], act, replace=False).astype(np.int32) for _ in range(9)]
     ids_dev = [up(np.asarray(i, dtype=np.int32), device) for i in id_sets]
-    ys = [torch.empty((w["n_active"], w["rows"]), dtype=torch.float32, device=device) for _ in id_sets]
+    ys = [torch.empty((act, w["rows"]), dtype=torch.float32, device=device) for _ in id_sets]
     calls = [lambda i=i: ops.mxfp4_expert_gemv(codes, scales, ids_dev[i], x, y=ys[i]) for i in range(len(id_sets))]
-    return dict(calls=calls, bytes=mxfp4_bytes(w["n_active"], w["rows"], w["cols"]), launches=1)
+    return dict(calls=calls, bytes=mxfp4_bytes(act, w["rows"], w["cols"]), launches=1)
 
 
 def summarize(st: dict, r: dict, steps: int, peak: float, sampler, **extra) -> dict:
@@ -472,11 +476,27 @@ def measure_extra(device, stream, world, peak, steps, warmup, sampler):
                 if k == 2 else "one launch on the CUDA cores: NVFP4 decoded in registers")
         ops.set_fp4_kernel(0)
         del st
+    # The MTP block's OCP MXFP4 experts (e8m0 per 32 columns), the same two
+    # kernels and by-shape routing.
     st = setup_mxfp4(device)
     r = time_reps(st["calls"], steps, warmup, stream, world, device)
     out["mxfp4_experts_6of64_2048x4096"] = summarize(
         st, r, steps, peak, sampler,
-        note="the MTP block's OCP MXFP4 experts: one launch, e8m0 per 32 columns decoded in registers")
+        note="the MTP block's OCP MXFP4 experts: one launch, the by-shape default (CUDA cores here)")
+    for act, name in ((6, "mxfp4_experts_6of64_2048x4096"), (64, "mxfp4_experts_64of64_2048x4096")):
+        if act != 6:
+            st = setup_mxfp4(device, act)
+        for k, arm in ((2, "_tensor_core"), (1, "_cuda_core")):
+            if act == 6 and k == 1:
+                continue
+            ops.set_fp4_kernel(k)
+            r = time_reps(st["calls"], steps, warmup, stream, world, device)
+            out[name + arm] = summarize(
+                st, r, steps, peak, sampler,
+                note="one launch on the tensor cores: e2m1 codes fed to tcgen05 kind::f8f6f4 as stored"
+                if k == 2 else "one launch on the CUDA cores: MXFP4 decoded in registers")
+        ops.set_fp4_kernel(0)
+        del st
     return with_traffic(out)
 
 
@@ -743,6 +763,8 @@ def run_profile_workload(args):
         st = setup_nvfp4(device, fused=not args.profile_workload.endswith("_two_step"))
     elif args.profile_workload == "nvfp4_experts_64of64_2048x4096":
         st = setup_nvfp4(device, True, 64)
+    elif args.profile_workload == "mxfp4_experts_64of64_2048x4096":
+        st = setup_mxfp4(device, 64)
     else:
         st = setup_fp8blk(args.profile_workload, device, args.profile_workload.startswith("head_argmax"))
     for i in range(args.calls):

@@ -145,12 +145,12 @@ cudaError_t weight_tensor_map(const uint8_t *w, int64_t rows, int64_t cols, int 
 }
 
 cudaError_t nvfp4_tensor_maps(const uint8_t *codes, const uint8_t *scales, int64_t total_rows, int64_t cols,
-                              int box_rows, CUtensorMap *cmap, CUtensorMap *smap) {
+                              int scale_block, int box_rows, CUtensorMap *cmap, CUtensorMap *smap) {
     const cudaError_t err = tensor_map_2d(codes, total_rows, cols, cols / 2, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B,
                                           box_rows, 128, CU_TENSOR_MAP_SWIZZLE_128B, cmap);
     if (err != cudaSuccess) return err;
-    return tensor_map_2d(scales, total_rows, cols / 16, cols / 16, CU_TENSOR_MAP_DATA_TYPE_UINT8, box_rows,
-                         kF4StageColsHost / 16, CU_TENSOR_MAP_SWIZZLE_NONE, smap);
+    return tensor_map_2d(scales, total_rows, cols / scale_block, cols / scale_block, CU_TENSOR_MAP_DATA_TYPE_UINT8,
+                         box_rows, 16, CU_TENSOR_MAP_SWIZZLE_NONE, smap);
 }
 
 static int pow2_floor(int v) {

@@ -129,9 +129,14 @@ __device__ __forceinline__ void f4_ld16(uint32_t taddr, uint32_t (&r)[16]) {
         : "r"(taddr));
 }
 
+template <int FP4>
 __global__ void __launch_bounds__(kF4Threads, 1)
     fp4tc_gemv_kernel(const __grid_constant__ CUtensorMap cmap, const __grid_constant__ CUtensorMap smap,
                       const F4Args a) {
+    // Scale blocks of SB columns: NVFP4 e4m3 per 16 (two blocks per K = 32
+    // step, block-diagonal B), MXFP4 e8m0 per 32 (one block per step).
+    constexpr bool kMx = FP4 == kFp4Mx;
+    constexpr int SB = fp4_scale_cols<FP4>();
     extern __shared__ __align__(1024) uint8_t f4_smem[];
     __shared__ __align__(8) uint64_t raw_full[kF4MaxRawStages], raw_free[kF4MaxRawStages];
     __shared__ __align__(8) uint64_t sc_full[kF4ScaleSlots], sc_free[kF4ScaleSlots];
@@ -209,7 +214,7 @@ __global__ void __launch_bounds__(kF4Threads, 1)
     bool p_ok = false;  // the unit's expert is usable
     NvSlot pcache;
     auto p_unit_start = [&]() {
-        const int e = nv_slot<kFp4Nv>(nv, p_k, pcache).e;
+        const int e = nv_slot<FP4>(nv, p_k, pcache).e;
         p_ok = e >= 0;
         p_row0 = p_ok ? static_cast<int>(static_cast<int64_t>(e) * nv.rows + p_slab * R) : 0;
     };
@@ -224,7 +229,7 @@ __global__ void __launch_bounds__(kF4Threads, 1)
             t8_tma_2d(smem_addr(st), &cmap, p_rs * kF4StageCols, p_row0, cbar, pol);
             t8_tma_2d(smem_addr(st + kF4RowSmem * R), &cmap, p_rs * kF4StageCols + kF4BoxCols, p_row0, cbar, pol);
             mbar_arrive_expect_tx(sbar, static_cast<uint32_t>(R) * 16);
-            t8_tma_2d(smem_addr(sSc + p_sslot * kF4ScaleSlotSmem), &smap, p_rs * (kF4StageCols / 16), p_row0, sbar,
+            t8_tma_2d(smem_addr(sSc + p_sslot * kF4ScaleSlotSmem), &smap, kMx ? (p_rs >> 1) * 16 : p_rs * 16, p_row0, sbar,
                       pol);
         }
         ++p_issued;
@@ -268,7 +273,7 @@ __global__ void __launch_bounds__(kF4Threads, 1)
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
             const int64_t c = c0 + static_cast<int64_t>(u) * 4 * kBThreads;
-            if (c >= nv.cols) break;  // the same for the four lanes of a block
+            if (c >= nv.cols) break;  // the same for the lanes of a block
             const float4 v = xv[u];
             auto fin = [](float f) {  // |f| as bits, 0 for inf / NaN
                 const uint32_t b = __float_as_uint(fabsf(f));
@@ -279,18 +284,20 @@ __global__ void __launch_bounds__(kF4Threads, 1)
                             fabsf(v.w) < INFINITY)
                                ? 0u
                                : 1u;
-            const uint32_t grp = 0xFu << (lane & ~3);
-            mx = max(mx, __shfl_xor_sync(grp, mx, 1));
-            mx = max(mx, __shfl_xor_sync(grp, mx, 2));
-            bad |= __shfl_xor_sync(grp, bad, 1);
-            bad |= __shfl_xor_sync(grp, bad, 2);
+            constexpr int GL = SB / 4;  // lanes per scale block
+            const uint32_t grp = ((1u << GL) - 1u) << (lane & ~(GL - 1));
+#pragma unroll
+            for (int o = 1; o < GL; o <<= 1) {
+                mx = max(mx, __shfl_xor_sync(grp, mx, o));
+                bad |= __shfl_xor_sync(grp, bad, o);
+            }
             const int eb = t8_plane_exponent(__uint_as_float(mx));  // 2^7 <= max |x| 2^eb < 2^8 (finite max)
             float f1, f2;
             t8_pow2_split(eb, f1, f2);
-            if ((lane & 3) == 0) {
+            if ((lane & (GL - 1)) == 0) {
                 float g1, g2;
                 t8_pow2_split(-eb, g1, g2);
-                sC[c >> 4] = bad ? __int_as_float(0x7FC00000) : g1 * g2;
+                sC[c / SB] = bad ? __int_as_float(0x7FC00000) : g1 * g2;
             }
             float t0 = bad ? 0.f : v.x * f1 * f2, t1 = bad ? 0.f : v.y * f1 * f2;
             float t2 = bad ? 0.f : v.z * f1 * f2, t3 = bad ? 0.f : v.w * f1 * f2;
@@ -302,7 +309,7 @@ __global__ void __launch_bounds__(kF4Threads, 1)
 #pragma unroll
             for (int p = 0; p < kF4Planes; ++p) {
                 const uint32_t lo = t8_to_e4m3x2(t0, t1), hi = t8_to_e4m3x2(t2, t3);
-                const int n = 5 * h + p;
+                const int n = kMx ? p : 5 * h + p;  // MXFP4: the step's one block spans both halves
                 *reinterpret_cast<uint32_t *>(bt + (n >> 3) * 1024 + (n & 7) * 128 + (((2 * j + h) ^ (n & 7)) << 4) +
                                               o) = lo | (hi << 16);
                 if (p + 1 < kF4Planes) {
@@ -391,7 +398,8 @@ __global__ void __launch_bounds__(kF4Threads, 1)
             float acc0 = 0.f, acc1 = 0.f;  // even and odd blocks
             for (int rs = 0; rs < nrs; ++rs, ++g) {
                 if ((g & 1u) != static_cast<uint32_t>(hf)) continue;
-                // This row's 16 block scales of the stage.
+                // This row's block scales of the stage: NVFP4 16 e4m3 bytes;
+                // MXFP4 8 e8m0 bytes, the stage pair's slot half (rs & 1).
                 const int ss = static_cast<int>(g % kF4ScaleSlots);
                 if (!f4_warp_wait(smem_addr(&sc_full[ss]), (g / kF4ScaleSlots) & 1u, &s_abort, lane)) {
                     stop = true;
@@ -408,7 +416,8 @@ __global__ void __launch_bounds__(kF4Threads, 1)
                 }
                 t8_fence_after();
                 const uint32_t sw[4] = {sc.x, sc.y, sc.z, sc.w};
-                const float *cb = sC + static_cast<size_t>(rs) * (kF4StageCols / 16);
+                const uint32_t mw0 = (rs & 1) ? sc.z : sc.x, mw1 = (rs & 1) ? sc.w : sc.y;  // MXFP4: this stage's 8 bytes
+                const float *cb = sC + static_cast<size_t>(rs) * (kF4StageCols / SB);
 #pragma unroll
                 for (int half = 0; half < 2; ++half) {
                     uint32_t d[kF4Steps / 2][16];
@@ -425,19 +434,31 @@ __global__ void __launch_bounds__(kF4Threads, 1)
                     }
 #pragma unroll
                     for (int t = 0; t < kF4Steps / 2; ++t) {
-                        // blocks 2T, 2T + 1 of the stage (T = 4 half + t): scale bytes 2T, 2T + 1
                         const int T = 4 * half + t;
-                        const float2 s2 = e4m3x2_to_f32((sw[T >> 1] >> (16 * (T & 1))) & 0xFFFFu);
-                        float u[2];
+                        if constexpr (kMx) {
+                            // block T of the stage: e8m0 byte 8 (rs & 1) + T of the slot row
+                            const uint32_t byte = ((T >> 2 ? mw1 : mw0) >> (8 * (T & 3))) & 0xFFu;
+                            float u = __uint_as_float(d[t][kF4Planes - 1]);
 #pragma unroll
-                        for (int hh = 0; hh < 2; ++hh) {
-                            u[hh] = __uint_as_float(d[t][5 * hh + kF4Planes - 1]);
+                            for (int p = kF4Planes - 2; p >= 0; --p) u = fmaf(u, 0.0625f, __uint_as_float(d[t][p]));
+                            if (T & 1)
+                                acc1 = fmaf(u, e8m0_to_f32(byte) * cb[T], acc1);
+                            else
+                                acc0 = fmaf(u, e8m0_to_f32(byte) * cb[T], acc0);
+                        } else {
+                            // blocks 2T, 2T + 1 of the stage: scale bytes 2T, 2T + 1
+                            const float2 s2 = e4m3x2_to_f32((sw[T >> 1] >> (16 * (T & 1))) & 0xFFFFu);
+                            float u[2];
 #pragma unroll
-                            for (int p = kF4Planes - 2; p >= 0; --p)
-                                u[hh] = fmaf(u[hh], 0.0625f, __uint_as_float(d[t][5 * hh + p]));
+                            for (int hh = 0; hh < 2; ++hh) {
+                                u[hh] = __uint_as_float(d[t][5 * hh + kF4Planes - 1]);
+#pragma unroll
+                                for (int p = kF4Planes - 2; p >= 0; --p)
+                                    u[hh] = fmaf(u[hh], 0.0625f, __uint_as_float(d[t][5 * hh + p]));
+                            }
+                            acc0 = fmaf(u[0], s2.x * cb[2 * T], acc0);
+                            acc1 = fmaf(u[1], s2.y * cb[2 * T + 1], acc1);
                         }
-                        acc0 = fmaf(u[0], s2.x * cb[2 * T], acc0);
-                        acc1 = fmaf(u[1], s2.y * cb[2 * T + 1], acc1);
                     }
                 }
             }
@@ -456,7 +477,7 @@ __global__ void __launch_bounds__(kF4Threads, 1)
                 const float total = part + sAcc[cbuf * 128 + r];
                 __syncwarp();
                 if (lane == 0) mbar_arrive(smem_addr(&comb_free[cbuf]));
-                const NvSlot &sl = nv_slot<kFp4Nv>(nv, k, cache);
+                const NvSlot &sl = nv_slot<FP4>(nv, k, cache);
                 const int64_t row = slab * R + r;
                 if (r < R && row < nv.rows)
                     nv.y[static_cast<int64_t>(k) * nv.rows + row] = sl.e >= 0 ? total * sl.g : __int_as_float(0x7FC00000);

@@ -74,13 +74,13 @@ void apply_plan(const Plan &p, GemvArgs *a);
 // {cols, rows}, boxes of box_rows rows x 128 bytes, 128-byte swizzle, zeros
 // out of range.  Cached per (pointer, shape, box height).
 cudaError_t weight_tensor_map(const uint8_t *w, int64_t rows, int64_t cols, int box_rows, CUtensorMap *out);
-// NVFP4 codes [total_rows, cols] e2m1 (boxes of box_rows x 128 codes, each
-// 8 code bytes landing in a 16-byte shared-memory chunk, 128-byte swizzle)
-// and e4m3 scales [total_rows, cols / 16] (box_rows x 16-byte boxes) for the
-// tensor-core FP4 kernel, which copies 256 columns per stage.
+// FP4 codes [total_rows, cols] e2m1 (boxes of box_rows x 128 codes, each 8
+// code bytes landing in a 16-byte shared-memory chunk, 128-byte swizzle) and
+// scales [total_rows, cols / scale_block] bytes (box_rows x 16-byte boxes)
+// for the tensor-core FP4 kernel, which copies 256 columns per stage.
 constexpr int kF4StageColsHost = 256;
 cudaError_t nvfp4_tensor_maps(const uint8_t *codes, const uint8_t *scales, int64_t total_rows, int64_t cols,
-                              int box_rows, CUtensorMap *cmap, CUtensorMap *smap);
+                              int scale_block, int box_rows, CUtensorMap *cmap, CUtensorMap *smap);
 
 // Kernel launches (defined in gemv_e4m3.cu / gemv_bf16.cu / nvfp4_dequant.cu /
 // gemv_tc.cu).

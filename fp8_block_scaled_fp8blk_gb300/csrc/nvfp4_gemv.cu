@@ -16,8 +16,9 @@ static int f4_slab_rows(const Nvfp4Args &a, const DeviceInfo &dev) {
     return 128;
 }
 
-// NVFP4 on the tensor cores: one CTA per SM over contiguous ranges of
+// FP4 experts on the tensor cores: one CTA per SM over contiguous ranges of
 // (slot, slab) units.
+template <int FP4>
 static cudaError_t launch_fp4tc(const Nvfp4Args &a, const DeviceInfo &dev, cudaStream_t stream) {
     F4Args f = {};
     f.nv = a;
@@ -28,11 +29,11 @@ static cudaError_t launch_fp4tc(const Nvfp4Args &a, const DeviceInfo &dev, cudaS
     f.units = f.n_slabs * a.n_active;
     CUtensorMap cmap, smap;
     cudaError_t err = nvfp4_tensor_maps(a.codes, a.scales, static_cast<int64_t>(a.n_experts) * a.rows, a.cols,
-                                        f.slab_rows, &cmap, &smap);
+                                        fp4_scale_cols<FP4>(), f.slab_rows, &cmap, &smap);
     if (err != cudaSuccess) return err;
     const size_t smem = f4_smem_bytes(a.cols, f.raw_stages, f.slab_rows);
     int per_sm = 0;
-    err = kernel_occupancy(reinterpret_cast<const void *>(fp4tc_gemv_kernel), kF4Threads, smem, &per_sm);
+    err = kernel_occupancy(reinterpret_cast<const void *>(fp4tc_gemv_kernel<FP4>), kF4Threads, smem, &per_sm);
     if (err != cudaSuccess) return err;
     if (per_sm < 1) return cudaErrorInvalidConfiguration;
     int64_t grid = dev.sms;
@@ -48,16 +49,16 @@ static cudaError_t launch_fp4tc(const Nvfp4Args &a, const DeviceInfo &dev, cudaS
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = tuning().use_pdl ? 1 : 0;
-    return cudaLaunchKernelEx(&cfg, fp4tc_gemv_kernel, cmap, smap, f);
+    return cudaLaunchKernelEx(&cfg, fp4tc_gemv_kernel<FP4>, cmap, smap, f);
 }
 
-// By shape, NVFP4 experts take the tensor cores from this many active rows
+// By shape, FP4 experts take the tensor cores from this many active rows
 // (n_active x rows) on: below it the slabs are too short for the per-stage
-// copies to reach the CUDA-core kernel's rate (6 x 2048 rows: 12.7 vs 12.5
-// us; 12 x 2048: 20.2 vs 21.5 us; 64 x 2048: 60.3 vs 86.3 us).
+// copies to reach the CUDA-core kernel's rate (NVFP4, 6 x 2048 rows: 12.7 vs
+// 12.5 us; 12 x 2048: 20.2 vs 21.5 us; 64 x 2048: 60.3 vs 86.3 us).
 constexpr int64_t kF4TcMinActiveRows = 16384;
 
-// NVFP4 experts take the tensor cores when chosen (by shape or pinned) and
+// FP4 experts take the tensor cores when chosen (by shape or pinned) and
 // the codes start on a 32-byte boundary (the packed-code TMA type), the slab
 // rows fit 32-bit TMA coordinates over the experts' stacked rows, and B plus
 // a minimal ring fit in shared memory.
@@ -70,7 +71,8 @@ static bool fp4_use_tensor_cores(const Nvfp4Args &a, const DeviceInfo &dev) {
 }
 
 cudaError_t launch_fp4_expert_gemv(Nvfp4Args a, bool mxfp4, const DeviceInfo &dev, cudaStream_t stream) {
-    if (!mxfp4 && fp4_use_tensor_cores(a, dev)) return launch_fp4tc(a, dev, stream);
+    if (fp4_use_tensor_cores(a, dev))
+        return mxfp4 ? launch_fp4tc<kFp4Mx>(a, dev, stream) : launch_fp4tc<kFp4Nv>(a, dev, stream);
     a.panels = static_cast<int>((a.cols + kNvMaxPanel - 1) / kNvMaxPanel);
     a.panel_cols = a.panels == 1 ? static_cast<int>(a.cols) : kNvMaxPanel;
     const int row_bytes = a.panel_cols / 2 + a.panel_cols / (mxfp4 ? 32 : 16);

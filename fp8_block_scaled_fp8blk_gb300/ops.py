@@ -255,7 +255,8 @@ def nvfp4_expert_gemv(codes: torch.Tensor, scales: torch.Tensor, gscale: torch.T
 def mxfp4_expert_gemv(codes: torch.Tensor, scales: torch.Tensor, ids: torch.Tensor, x: torch.Tensor,
                       y: torch.Tensor | None = None) -> torch.Tensor:
     """OCP MXFP4 experts: y [n_active, rows] = W(ids[k]) x in one launch
-    (e8m0 scale per 32 columns, decoded in registers; `ids` int32 on the device)."""
+    (e8m0 scale per 32 columns; CUDA cores or tensor cores, see
+    set_fp4_kernel; `ids` int32 on the device)."""
     n_experts, rows, half = codes.shape
     cols = 2 * half
     if ids.dtype != torch.int32:
@@ -295,8 +296,8 @@ def set_m1_kernel(choice: int = 0, rowwarp_min_bytes: int = 0) -> None:
 
 
 def set_fp4_kernel(choice: int = 0) -> None:
-    """NVFP4 expert GEMV kernel: 0 by shape (tensor cores from 16384 active
-    rows on), 1 CUDA cores, 2 tensor cores."""
+    """NVFP4 and MXFP4 expert GEMV kernel: 0 by shape (tensor cores from
+    16384 active rows on), 1 CUDA cores, 2 tensor cores."""
     _check(_lib.fp8blk_set_fp4_kernel(choice), "fp8blk_set_fp4_kernel")
 
 

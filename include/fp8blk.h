@@ -253,6 +253,9 @@ int nvfp4_expert_gemv(const uint8_t *codes, const uint8_t *scales, const float *
  * mxfp4_expert_gemv -- as nvfp4_expert_gemv, for OCP MXFP4 experts (the MTP
  * block's routed experts, "Module dsv4_gpu" page, enum ExpertKind):
  *   y[k][r] = sum_c e2m1(q[e][r][c]) * 2^(s[e][r][c/32] - 127) * x[c], e = ids[k].
+ * Same two kernels and routing as nvfp4_expert_gemv (fp8blk_set_fp4_kernel);
+ * on the tensor cores x is split into five e4m3 planes per 32-column block and
+ * each 32-column block sum is scaled by its e8m0 factor.
  * The page names the format only; the layout is read from the OCP MX format:
  *   codes        device, uint8 [n_experts, rows, cols/2], two e2m1 codes per
  *                byte, column 2j in the LOW nibble; 16-byte aligned
@@ -261,7 +264,8 @@ int nvfp4_expert_gemv(const uint8_t *codes, const uint8_t *scales, const float *
  *   ids          DEVICE, int32 [n_active]; repeats allowed
  *   cols         a multiple of 512 (so every scale row starts on 16 bytes).
  * No global scale.  An id outside [0, n_experts) sets
- * FP8BLK_STATUS_BAD_EXPERT and makes y[k] NaN.
+ * FP8BLK_STATUS_BAD_EXPERT and makes y[k] NaN.  An inf or NaN in x: the
+ * CUDA cores give the IEEE result, the tensor cores NaN in every output.
  * Errors: EINVAL, EALIGN, ERANGE, ECUDA.
  */
 int mxfp4_expert_gemv(const uint8_t *codes, const uint8_t *scales, int n_experts, const int32_t *ids,
@@ -318,18 +322,20 @@ int fp8blk_set_wait_limit(int64_t limit_ns);
 int fp8blk_set_m1_kernel(int choice, int64_t rowwarp_min_bytes);
 
 /*
- * fp8blk_set_fp4_kernel -- which kernel serves nvfp4_expert_gemv (speed only;
+ * fp8blk_set_fp4_kernel -- which kernel serves nvfp4_expert_gemv and
+ * mxfp4_expert_gemv (speed only;
  * both are within the stated error bound, each bit-identical run to run):
  *   0 = by shape: the tensor cores from 16384 active rows (n_active x rows)
  *   on, the CUDA cores below; 1 = CUDA cores (weights decoded to f32 in
  *   registers, one f32 FMA each); 2 = tensor cores (the e2m1 codes fed to
- *   tcgen05.mma kind::f8f6f4 as stored, x as five e4m3 planes per 16-column
- *   block, the block scales applied to the f32 block sums).  The tensor
+ *   tcgen05.mma kind::f8f6f4 as stored, x as five e4m3 planes per scale
+ *   block -- 16 columns NVFP4, 32 MXFP4 -- the block scales applied to the
+ *   f32 block sums).  The tensor
  *   cores also need 32-byte-aligned codes and room in shared memory for x's
  *   planes (16 bytes per column) beside three stages (cols up to 6656 with
  *   128-row slabs), else the CUDA cores serve the call; with an inf or NaN in
  *   x they return NaN in every output, the CUDA cores the IEEE result.
- *   mxfp4_expert_gemv always runs on the CUDA cores.  Errors: EINVAL.
+ *   Errors: EINVAL.
  */
 int fp8blk_set_fp4_kernel(int choice);
 

@@ -1,5 +1,6 @@
 """GPU parity of the one-launch OCP MXFP4 routed-expert GEMV (the MTP block's
-experts) against the CPU oracle, through the C ABI.
+experts) against the CPU oracle, through the C ABI, on both kernels (CUDA
+cores and tensor cores).
 
 Bar: outputs within |gpu - oracle| <= 1e-5 * sum|w x| + 1e-6; one-hot x
 reproduces every decoded weight exactly (e2m1 code x e8m0 scale); a 0xFF
@@ -24,6 +25,13 @@ def ops():
     assert o.fp8blk_device_status(clear=True) == 0
 
 
+@pytest.fixture(params=[1, 2], ids=["cuda_cores", "tensor_cores"])
+def fp4k(ops, request):
+    ops.set_fp4_kernel(request.param)
+    yield request.param
+    ops.set_fp4_kernel(0)
+
+
 def run(ops, case, ids=None, x=None):
     ids = case.ids if ids is None else ids
     x = case.x if x is None else x
@@ -33,7 +41,7 @@ def run(ops, case, ids=None, x=None):
     return y.cpu().numpy()
 
 
-def test_mxfp4_full_config(ops):
+def test_mxfp4_full_config(ops, fp4k):
     w = synth.MXFP4_WORKLOAD
     case = synth.mxfp4_case(w["n_experts"], w["rows"], w["cols"], w["n_active"], w["seed"])
     y = run(ops, case)
@@ -43,14 +51,14 @@ def test_mxfp4_full_config(ops):
 
 @pytest.mark.parametrize("n_experts,rows,cols,n_active", [(3, 1, 512, 1), (4, 7, 1024, 2), (8, 129, 4096, 3),
                                                           (5, 1000, 1536, 5), (6, 130, 4608, 4), (4, 65, 8192, 4)])
-def test_mxfp4_ragged(ops, n_experts, rows, cols, n_active):
+def test_mxfp4_ragged(ops, fp4k, n_experts, rows, cols, n_active):
     case = synth.mxfp4_case(n_experts, rows, cols, n_active, seed=rows * 17 + cols + n_active)
     y = run(ops, case)
     ref, a = oracle.mxfp4_expert_gemv(case.codes, case.scales, case.ids, case.x, nthreads=8)
     assert_close(y, ref, a, f"mxfp4 {n_experts}x{rows}x{cols} k={n_active}")
 
 
-def test_mxfp4_one_hot_is_exact(ops):
+def test_mxfp4_one_hot_is_exact(ops, fp4k):
     """Every e2m1 code under e8m0 scales from 2^-127 to 2^127: x = e_c returns
     the decoded weight column exactly."""
     rows, cols = 8, 512
@@ -67,16 +75,52 @@ def test_mxfp4_one_hot_is_exact(ops):
         assert np.array_equal(y[0], want), c
 
 
-def test_mxfp4_scale_ff_poisons_only_its_row(ops):
+def test_mxfp4_scale_ff_poisons_only_its_row(ops, fp4k):
     case = synth.mxfp4_case(3, 40, 1024, 2, seed=9)
     case.scales[case.ids[1], 17, 5] = 0xFF
     y = run(ops, case)
     assert np.isnan(y[1, 17]) and not np.isnan(np.delete(y[1], 17)).any() and not np.isnan(y[0]).any()
 
 
-def test_mxfp4_bad_and_repeated_ids(ops):
+def test_mxfp4_bad_and_repeated_ids(ops, fp4k):
     case = synth.mxfp4_case(4, 100, 512, 3, seed=10)
     assert ops.fp8blk_device_status(clear=True) == 0
     y = run(ops, case, ids=[2, 7, 2])
     assert np.isnan(y[1]).all() and np.array_equal(y[0], y[2])
     assert ops.fp8blk_device_status(clear=True) == ops.STATUS_BAD_EXPERT
+
+
+def test_mxfp4_x_inf_and_nan(ops, fp4k):
+    """An inf in x: the CUDA-core arm gives +-inf where its weight is nonzero
+    and NaN where it is zero (0 * inf), as the oracle does; the tensor-core arm
+    gives NaN everywhere (its x planes cannot hold an inf, so the non-finite
+    32-column block poisons every sum).  A NaN in x makes every output NaN."""
+    case = synth.mxfp4_case(2, 256, 1024, 2, seed=83)
+    x = case.x.copy()
+    x[100] = np.inf
+    x[700] = 1e30
+    y = run(ops, case, x=x)
+    ref, _ = oracle.mxfp4_expert_gemv(case.codes, case.scales, case.ids, x, nthreads=8)
+    assert np.isnan(ref).any() and np.isinf(ref).any() and not np.isfinite(ref).any()
+    if fp4k == 1:
+        assert np.array_equal(np.isnan(y), np.isnan(ref))
+        assert np.array_equal(y[~np.isnan(ref)], ref[~np.isnan(ref)])
+    else:
+        assert np.isnan(y).all()
+    x[5] = np.nan
+    assert np.isnan(run(ops, case, x=x)).all()
+
+
+def test_mxfp4_kernels_agree_many_active(ops):
+    """32 of 64 experts active (the tensor cores' by-shape regime): the default
+    gives the tensor-core kernel's bits, and both kernels meet the bound."""
+    case = synth.mxfp4_case(64, 1024, 2048, 32, seed=11)
+    runs = {}
+    for k in (0, 1, 2):
+        ops.set_fp4_kernel(k)
+        runs[k] = run(ops, case)
+    ops.set_fp4_kernel(0)
+    assert np.array_equal(runs[0].view(np.uint32), runs[2].view(np.uint32))
+    ref, a = oracle.mxfp4_expert_gemv(case.codes, case.scales, case.ids, case.x, nthreads=16)
+    for k in (1, 2):
+        assert_close(runs[k], ref, a, f"mxfp4 32 of 64, kernel {k}")
