@@ -24,9 +24,13 @@
 //   once per CTA for all of x.
 // D (TMEM): 16 columns per step, eight steps per 256-column stage, a ring of
 //   four stages (512 columns).  The epilogue forms per row
-//   acc += (sum_p D[b][p] 2^-4p) * e4m3(s[r][b]) * 2^-e_b   (f32),
+//   acc += e4m3(s[r][b]) * ((sum_p D[b][p] 2^-4p) * 2^-e_b)   (f32),
 //   in block order within four sums (even / odd blocks of even / odd
-//   stages), added in a fixed order at the end.
+//   stages), added in a fixed order at the end.  The inner product by the
+//   power of two is exact: it is the block sum in x's units, so the scale is
+//   applied to the same value as on the CUDA cores, and a block of zero codes
+//   adds zero whatever its scale and x (the other grouping could form
+//   scale * 2^-e_b = inf and then 0 * inf).
 //
 // Work: units (active slot, R-row slab of the expert, R <= 128 chosen on the
 // host so the units fill the SMs), contiguous ranges per CTA; an MMA always
@@ -127,6 +131,14 @@ __device__ __forceinline__ void f4_ld16(uint32_t taddr, uint32_t (&r)[16]) {
         : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
           "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
         : "r"(taddr));
+}
+
+// TMEM -> registers: 8 consecutive 32-bit columns of the warp's 32 lanes
+// (MXFP4 uses 5 of a step's 16 columns).
+__device__ __forceinline__ void f4_ld8(uint32_t taddr, uint32_t (&r)[8]) {
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+                 : "r"(taddr));
 }
 
 template <int FP4>
@@ -420,12 +432,17 @@ __global__ void __launch_bounds__(kF4Threads, 1)
                 const float *cb = sC + static_cast<size_t>(rs) * (kF4StageCols / SB);
 #pragma unroll
                 for (int half = 0; half < 2; ++half) {
-                    uint32_t d[kF4Steps / 2][16];
+                    // NVFP4 reads a step's ten plane sums, MXFP4 its five
+                    uint32_t d[kF4Steps / 2][kMx ? 8 : 16];
 #pragma unroll
-                    for (int t = 0; t < kF4Steps / 2; ++t)
-                        f4_ld16(tmem + static_cast<uint32_t>(ds * 128 + 16 * (4 * half + t)) +
-                                    (static_cast<uint32_t>(qr * 32) << 16),
-                                d[t]);
+                    for (int t = 0; t < kF4Steps / 2; ++t) {
+                        const uint32_t ta = tmem + static_cast<uint32_t>(ds * 128 + 16 * (4 * half + t)) +
+                                            (static_cast<uint32_t>(qr * 32) << 16);
+                        if constexpr (kMx)
+                            f4_ld8(ta, d[t]);
+                        else
+                            f4_ld16(ta, d[t]);
+                    }
                     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
                     if (half == 1) {
                         t8_fence_before();
@@ -441,10 +458,12 @@ __global__ void __launch_bounds__(kF4Threads, 1)
                             float u = __uint_as_float(d[t][kF4Planes - 1]);
 #pragma unroll
                             for (int p = kF4Planes - 2; p >= 0; --p) u = fmaf(u, 0.0625f, __uint_as_float(d[t][p]));
+                            // u * 2^-e_b is exact (a power of two): the block sum
+                            // in x's units, scaled as the CUDA-core kernel does
                             if (T & 1)
-                                acc1 = fmaf(u, e8m0_to_f32(byte) * cb[T], acc1);
+                                acc1 = fmaf(e8m0_to_f32(byte), u * cb[T], acc1);
                             else
-                                acc0 = fmaf(u, e8m0_to_f32(byte) * cb[T], acc0);
+                                acc0 = fmaf(e8m0_to_f32(byte), u * cb[T], acc0);
                         } else {
                             // blocks 2T, 2T + 1 of the stage: scale bytes 2T, 2T + 1
                             const float2 s2 = e4m3x2_to_f32((sw[T >> 1] >> (16 * (T & 1))) & 0xFFFFu);
@@ -456,8 +475,8 @@ __global__ void __launch_bounds__(kF4Threads, 1)
                                 for (int p = kF4Planes - 2; p >= 0; --p)
                                     u[hh] = fmaf(u[hh], 0.0625f, __uint_as_float(d[t][5 * hh + p]));
                             }
-                            acc0 = fmaf(u[0], s2.x * cb[2 * T], acc0);
-                            acc1 = fmaf(u[1], s2.y * cb[2 * T + 1], acc1);
+                            acc0 = fmaf(s2.x, u[0] * cb[2 * T], acc0);
+                            acc1 = fmaf(s2.y, u[1] * cb[2 * T + 1], acc1);
                         }
                     }
                 }

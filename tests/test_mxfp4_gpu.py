@@ -124,3 +124,80 @@ def test_mxfp4_kernels_agree_many_active(ops):
     ref, a = oracle.mxfp4_expert_gemv(case.codes, case.scales, case.ids, case.x, nthreads=16)
     for k in (1, 2):
         assert_close(runs[k], ref, a, f"mxfp4 32 of 64, kernel {k}")
+
+
+def test_mxfp4_x_wide_dynamic_range(ops, fp4k):
+    """x spanning 2^-40 .. 2^20: the f32 block sums keep the small terms' share
+    (on the tensor cores each 32-column block has its own plane exponent)."""
+    case = synth.mxfp4_case(3, 256, 2048, 2, seed=89)
+    rng = np.random.default_rng(90)
+    x = (rng.standard_normal(2048) * np.exp2(rng.integers(-40, 21, 2048))).astype(np.float32)
+    y = run(ops, case, x=x)
+    ref, a = oracle.mxfp4_expert_gemv(case.codes, case.scales, case.ids, x, nthreads=8)
+    assert_close(y, ref, a, "mxfp4 wide x")
+
+
+def test_mxfp4_scales_across_the_e8m0_range(ops, fp4k):
+    """Random codes and x under e8m0 scales drawn from 2^-127 .. 2^100 (every
+    output stays finite in f32): the block factors are applied to the f32 block
+    sums without overflow or loss beyond the bound."""
+    case = synth.mxfp4_case(2, 384, 1536, 2, seed=91)
+    rng = np.random.default_rng(92)
+    case.scales[:] = rng.choice(np.array([0, 1, 2, 60, 100, 126, 127, 128, 160, 200, 227], dtype=np.uint8),
+                                size=case.scales.shape)
+    y = run(ops, case)
+    ref, a = oracle.mxfp4_expert_gemv(case.codes, case.scales, case.ids, case.x, nthreads=8)
+    assert np.isfinite(ref).all() and np.isfinite(y).all()
+    assert_close(y, ref, a, "mxfp4 e8m0 range")
+
+
+def test_mxfp4_bit_identical_rerun(ops, fp4k):
+    """Two calls on the same inputs give the same bits (fixed reduction order)."""
+    w = synth.MXFP4_WORKLOAD
+    case = synth.mxfp4_case(w["n_experts"], w["rows"], w["cols"], w["n_active"], w["seed"])
+    y1, y2 = run(ops, case), run(ops, case)
+    assert np.array_equal(y1.view(np.uint32), y2.view(np.uint32))
+
+
+def test_mxfp4_tensor_cores_replayed_from_a_cuda_graph(ops):
+    """The MXFP4 tensor-core GEMV recorded into a CUDA graph and replayed on new
+    activations and new device ids gives the eager call's bits."""
+    case = synth.mxfp4_case(16, 2048, 1024, 8, seed=93)
+    codes, scales = to_dev(case.codes), to_dev(case.scales)
+    rng = np.random.default_rng(94)
+    ids_l = [np.asarray(case.ids, dtype=np.int32)] + [rng.choice(16, 8, replace=False).astype(np.int32)
+                                                       for _ in range(2)]
+    xs = [to_dev(case.x)] + [to_dev(rng.standard_normal(1024, dtype=np.float32)) for _ in range(2)]
+    ids_buf, x_buf = to_dev(ids_l[0]).clone(), xs[0].clone()
+    y = torch.empty((8, 2048), dtype=torch.float32, device="cuda:0")
+    ops.set_fp4_kernel(2)
+    try:
+        ops.mxfp4_expert_gemv(codes, scales, ids_buf, x_buf, y=y)  # per-shape host state outside the capture
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            ops.mxfp4_expert_gemv(codes, scales, ids_buf, x_buf, y=y)
+        for ids, x in zip(ids_l, xs):
+            ids_buf.copy_(to_dev(ids))
+            x_buf.copy_(x)
+            graph.replay()
+            torch.cuda.synchronize()
+            assert torch.equal(y, ops.mxfp4_expert_gemv(codes, scales, to_dev(ids), x))
+    finally:
+        ops.set_fp4_kernel(0)
+    assert ops.fp8blk_device_status(clear=True) == 0
+
+
+def test_mxfp4_zero_block_under_large_scale_and_x(ops, fp4k):
+    """A block of zero codes under the largest e8m0 scale (2^127), holding an x
+    of 1e6: it adds exactly zero, so every output is finite and meets the bound
+    (the scale must not meet x's magnitude before the zero block sum does)."""
+    case = synth.mxfp4_case(2, 96, 512, 2, seed=95)
+    case.codes[:, :, 0:16] = 0           # columns 0..31 (block 0) of every row: +0
+    case.scales[:, :, 0] = 254           # 2^127
+    x = case.x.copy()
+    x[3] = 1e6
+    y = run(ops, case, x=x)
+    ref, a = oracle.mxfp4_expert_gemv(case.codes, case.scales, case.ids, x, nthreads=8)
+    assert np.isfinite(ref).all() and np.isfinite(y).all()
+    assert_close(y, ref, a, "mxfp4 zero block, scale 2^127, x 1e6")

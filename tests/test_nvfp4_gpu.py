@@ -74,13 +74,15 @@ def test_expert_dequant_gemv_ragged(ops):
 
 
 # ---- one-launch expert GEMV, ids on the device: NVFP4 decoded in registers
-# (CUDA cores) or into exact f16 tiles for kind::f16 MMAs (tensor cores)
+# (CUDA cores) or the e2m1 codes fed to kind::f8f6f4 MMAs as stored, x as e4m3
+# planes per 16-column block (tensor cores)
 
 @pytest.fixture(params=[1, 2], ids=["cuda_cores", "tensor_cores"])
 def fp4k(ops, request):
     ops.set_fp4_kernel(request.param)
     yield request.param
     ops.set_fp4_kernel(0)
+
 
 def fused(ops, case, ids=None, gscale=None, status=0):
     """One call into a NaN-filled output; the device status word must then
@@ -153,9 +155,9 @@ def test_fused_matches_two_step_path(ops, fp4k, c5):
 
 
 def test_fused_x_wide_dynamic_range(ops, fp4k):
-    """x spanning 2^-40 .. 2^20: the f32 sums keep the small terms' share (the
-    tensor-core arm's f16 planes are scaled by max|x|; small entries sit far
-    below it)."""
+    """x spanning 2^-40 .. 2^20: the f32 sums keep the small terms' share (on
+    the tensor cores each 16-column block has its own plane exponent, so a
+    small entry is only cut relative to its block's maximum)."""
     case = synth.nvfp4_case(3, 256, 2048, 2, seed=77)
     rng = np.random.default_rng(78)
     x = (rng.standard_normal(2048) * np.exp2(rng.integers(-40, 21, 2048))).astype(np.float32)
@@ -179,6 +181,24 @@ def test_fused_nan_scale_poisons_only_its_row(ops, fp4k):
     ok[1, 133] = False
     ref, a, _ = oracle.nvfp4_expert_dequant_gemv(case.codes, case.scales, case.gscale, case.ids, case.x, nthreads=8)
     assert_close(y[ok], ref[ok], a[ok], "rows next to the NaN scale")
+
+
+def test_fused_zero_block_under_large_scale_and_x(ops, fp4k):
+    """A block of zero codes under the largest e4m3 scale (448), holding an x
+    of 3e38: it adds exactly zero, so every output is finite and meets the
+    bound (the scale must not meet x's magnitude before the zero block sum
+    does)."""
+    case = synth.nvfp4_case(2, 96, 512, 2, seed=96)
+    codes, scales = case.codes.copy(), case.scales.copy()
+    codes[:, :, 0:8] = 0                 # columns 0..15 (block 0) of every row: +0
+    scales[:, :, 0] = 0x7E               # 448
+    x = case.x.copy()
+    x[3] = 3e38
+    cx = synth.Nvfp4Case(codes, scales, case.gscale, case.ids, x)
+    y = fused(ops, cx)
+    ref, a, _ = oracle.nvfp4_expert_dequant_gemv(cx.codes, cx.scales, cx.gscale, cx.ids, cx.x, nthreads=8)
+    assert np.isfinite(ref).all() and np.isfinite(y).all()
+    assert_close(y, ref, a, "nvfp4 zero block, scale 448, x 3e38")
 
 
 def test_fused_bit_identical_rerun(ops, fp4k, c5):
