@@ -45,9 +45,11 @@
 //               a row meet in shared memory at the end of the unit; warp 0
 //               allocates and frees tensor memory;
 //   warp 8      TMA producer (one lane);
-//   warps 9-12  MMA issuers (one lane each): warp 9 + i issues steps 2i, 2i + 1
-//               of every stage (a single issuing thread is the bottleneck
-//               otherwise).
+//   warps 9-12  MMA issuers (one lane each): warp 9 + i issues the eight
+//               steps of every stage g with g % 4 == i, into D stage i (a
+//               thread issues tcgen05 ops at about 100 ns each, so four
+//               threads on whole stages, two commits per stage, beat any
+//               split of a stage's steps).
 // An expert id outside [0, n_experts) or an unusable global scale makes the
 // slot's outputs NaN and sets FP8BLK_STATUS_BAD_EXPERT; an inf or NaN in x
 // makes every output NaN (the exact sums are not finite).  Every wait is
@@ -73,12 +75,17 @@ constexpr int kF4N = 16;
 constexpr int kF4BTileBytes = kF4N * 128;                      // B for 128 columns (four steps)
 constexpr int kF4DStages = 4;                                  // D ring: 4 x 128 columns
 constexpr int kF4MaxRawStages = 8;
-constexpr int kF4MinRawStages = 3;
+constexpr int kF4MinRawStages = 4;
 constexpr int kF4EpiWarps = 8;                                 // two groups of four (even / odd stages)
 constexpr int kF4ProducerWarp = 8;
 constexpr int kF4MmaWarp0 = 9;
-constexpr int kF4Issuers = 4;
+constexpr int kF4Issuers = 4;                                  // issuer i: the stages g with g % 4 == i
 constexpr int kF4Threads = (kF4MmaWarp0 + kF4Issuers) * 32;
+// Issuer i owns D stage i and the code slots i, i + 4: it alone waits on and
+// commits to their barriers, in stage order, so no parity wait can be met by
+// an older phase.  Hence a ring of 4 or 8 stages.
+static_assert(kF4DStages == kF4Issuers && kF4MaxRawStages % kF4Issuers == 0 && kF4MinRawStages == kF4Issuers,
+              "issuers own their D stage and code slots");
 constexpr int kF4TmemCols = 512;
 constexpr uint32_t kF4IDesc = t8_idesc(128, kF4N) | (5u << 7);  // A e2m1 (format 5), B e4m3, D f32
 
@@ -98,10 +105,13 @@ __host__ __device__ constexpr size_t f4_smem_bytes(int64_t cols, int raw_stages,
     return f4_smem_need(cols, raw_stages, slab_rows) < 116 * 1024 ? 116 * 1024
                                                                   : f4_smem_need(cols, raw_stages, slab_rows);
 }
+// Code ring depth for a budget: the most stages that fit, at most
+// kF4MaxRawStages, rounded down to a multiple of kF4Issuers (0 if under 4).
 __host__ __device__ constexpr int f4_raw_stages(int64_t cols, int slab_rows, int64_t budget) {
-    return (budget - kF4FixedSmem - 16 * cols - cols / 4) / f4_stage_smem(slab_rows) > kF4MaxRawStages
-               ? kF4MaxRawStages
-               : static_cast<int>((budget - kF4FixedSmem - 16 * cols - cols / 4) / f4_stage_smem(slab_rows));
+    return ((budget - kF4FixedSmem - 16 * cols - cols / 4) / f4_stage_smem(slab_rows) > kF4MaxRawStages
+                ? kF4MaxRawStages
+                : static_cast<int>((budget - kF4FixedSmem - 16 * cols - cols / 4) / f4_stage_smem(slab_rows))) /
+           kF4Issuers * kF4Issuers;
 }
 
 struct F4Args {
@@ -181,14 +191,14 @@ __global__ void __launch_bounds__(kF4Threads, 1)
     if (tid == 0) {
         for (int s = 0; s < RS; ++s) {
             mbar_init(smem_addr(&raw_full[s]), 1);
-            mbar_init(smem_addr(&raw_free[s]), kF4Issuers);
+            mbar_init(smem_addr(&raw_free[s]), 1);  // the stage's issuer
         }
         for (int s = 0; s < kF4ScaleSlots; ++s) {
             mbar_init(smem_addr(&sc_full[s]), 1);
             mbar_init(smem_addr(&sc_free[s]), kF4EpiWarps / 2);  // one epilogue group per stage
         }
         for (int j = 0; j < kF4DStages; ++j) {
-            mbar_init(smem_addr(&d_full[j]), kF4Issuers);
+            mbar_init(smem_addr(&d_full[j]), 1);  // issuer j
             mbar_init(smem_addr(&d_free[j]), kF4EpiWarps / 2);
         }
         for (int j = 0; j < 2; ++j) {
@@ -355,34 +365,38 @@ __global__ void __launch_bounds__(kF4Threads, 1)
                 (void)mbar_wait_bounded(smem_addr(&sc_full[w % kF4ScaleSlots]), (w / kF4ScaleSlots) & 1u);
         }
     } else if (warp >= kF4MmaWarp0) {
-        // ---------------- MMA issuer i: steps 2i, 2i + 1 of every stage
+        // ---------------- MMA issuer i: all steps of the stages g with
+        // g % kF4Issuers == i, one commit per barrier per stage.  Issuing
+        // threads run in parallel on different stages: a thread's tcgen05
+        // ops, not the tensor pipe, set the rate.
         const int iss = warp - kF4MmaWarp0;
         if (lane == 0) {
             int slot = 0;
-            uint32_t pass = 0, g = 0;  // ring pass; stages issued
+            uint32_t pass = 0, g = 0;  // ring pass; stages so far
             bool stop = false;
             for (int i = 0; i < n_units && !stop; ++i) {
                 for (int rs = 0; rs < nrs; ++rs, ++g) {
-                    const int ds = static_cast<int>(g % kF4DStages);
-                    if (!f4_wait(smem_addr(&raw_full[slot]), pass & 1u, &s_abort) ||
-                        (g >= kF4DStages &&
-                         !f4_wait(smem_addr(&d_free[ds]), ((g / kF4DStages) - 1u) & 1u, &s_abort))) {
-                        stop = true;
-                        break;
-                    }
-                    t8_fence_after();
-                    const uint32_t st = smem_addr(sRaw + static_cast<size_t>(slot) * stage_smem);
+                    if (static_cast<int>(g % kF4Issuers) == iss) {
+                        const int ds = iss;  // g % kF4DStages
+                        if (!f4_wait(smem_addr(&raw_full[slot]), pass & 1u, &s_abort) ||
+                            (g >= kF4DStages &&
+                             !f4_wait(smem_addr(&d_free[ds]), ((g / kF4DStages) - 1u) & 1u, &s_abort))) {
+                            stop = true;
+                            break;
+                        }
+                        t8_fence_after();
+                        const uint32_t st = smem_addr(sRaw + static_cast<size_t>(slot) * stage_smem);
 #pragma unroll
-                    for (int q = 0; q < 2; ++q) {
-                        const int t = 2 * iss + q;  // step: code box t / 4, K offset 32 (t % 4) bytes
-                        const int box = t >> 2, kk = t & 3;
-                        const uint32_t bt = smem_addr(sB + static_cast<size_t>(2 * rs + box) * kF4BTileBytes);
-                        t8_mma(tmem + static_cast<uint32_t>(ds * 128 + 16 * t),
-                               t8_desc_sw128(st + box * kF4RowSmem * R + 32u * kk), t8_desc_sw128(bt + 32u * kk), kF4IDesc,
-                               false);
+                        for (int t = 0; t < kF4Steps; ++t) {  // step: code box t / 4, K offset 32 (t % 4) bytes
+                            const int box = t >> 2, kk = t & 3;
+                            const uint32_t bt = smem_addr(sB + static_cast<size_t>(2 * rs + box) * kF4BTileBytes);
+                            t8_mma(tmem + static_cast<uint32_t>(ds * 128 + 16 * t),
+                                   t8_desc_sw128(st + box * kF4RowSmem * R + 32u * kk), t8_desc_sw128(bt + 32u * kk),
+                                   kF4IDesc, false);
+                        }
+                        t8_commit(smem_addr(&raw_free[slot]));
+                        t8_commit(smem_addr(&d_full[ds]));
                     }
-                    t8_commit(smem_addr(&raw_free[slot]));
-                    t8_commit(smem_addr(&d_full[ds]));
                     if (++slot == RS) {
                         slot = 0;
                         ++pass;

@@ -53,10 +53,12 @@ static cudaError_t launch_fp4tc(const Nvfp4Args &a, const DeviceInfo &dev, cudaS
 }
 
 // By shape, FP4 experts take the tensor cores from this many active rows
-// (n_active x rows) on: below it the slabs are too short for the per-stage
-// copies to reach the CUDA-core kernel's rate (NVFP4, 6 x 2048 rows: 12.7 vs
-// 12.5 us; 12 x 2048: 20.2 vs 21.5 us; 64 x 2048: 60.3 vs 86.3 us).
-constexpr int64_t kF4TcMinActiveRows = 16384;
+// (n_active x rows) on.  The tensor-core kernel costs about 0.5 us per
+// 256-column stage however short its slab, so below it the CUDA-core kernel
+// is faster (2048 x 4096 experts, us, tensor vs CUDA cores: NVFP4 4 active
+// about 12.3 vs 9.2, 6 active 12.2 vs 12.5, 64 active 60.1 vs 86.3; MXFP4
+// 6 active 11.9 vs 12.8).
+constexpr int64_t kF4TcMinActiveRows = 12288;
 
 // FP4 experts take the tensor cores when chosen (by shape or pinned) and
 // the codes start on a 32-byte boundary (the packed-code TMA type), the slab

@@ -297,7 +297,7 @@ def set_m1_kernel(choice: int = 0, rowwarp_min_bytes: int = 0) -> None:
 
 def set_fp4_kernel(choice: int = 0) -> None:
     """NVFP4 and MXFP4 expert GEMV kernel: 0 by shape (tensor cores from
-    16384 active rows on), 1 CUDA cores, 2 tensor cores."""
+    12288 active rows on), 1 CUDA cores, 2 tensor cores."""
     _check(_lib.fp8blk_set_fp4_kernel(choice), "fp8blk_set_fp4_kernel")
 
 

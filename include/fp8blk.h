@@ -222,7 +222,7 @@ int nvfp4_expert_dequant_gemv(const uint8_t *codes, const uint8_t *scales,
  *   y[k][r] = sum_c bf16(e2m1(q[e][r][c]) * e4m3(s[e][r][c/16]) * g[e]) * x[c],
  *   e = ids[k]; every product is exact, so the weights take the same values
  *   as nvfp4_expert_dequant writes; the sum is in f32.  Two kernels
- *   (fp8blk_set_fp4_kernel; by shape, the tensor cores from 16384 active rows
+ *   (fp8blk_set_fp4_kernel; by shape, the tensor cores from 12288 active rows
  *   on): the CUDA cores decode the weights in registers; the tensor cores take
  *   the codes as stored, x as five e4m3 planes per 16-column block (2^-20 of
  *   each element), and apply the block scales to the f32 block sums.  Both
@@ -325,7 +325,7 @@ int fp8blk_set_m1_kernel(int choice, int64_t rowwarp_min_bytes);
  * fp8blk_set_fp4_kernel -- which kernel serves nvfp4_expert_gemv and
  * mxfp4_expert_gemv (speed only;
  * both are within the stated error bound, each bit-identical run to run):
- *   0 = by shape: the tensor cores from 16384 active rows (n_active x rows)
+ *   0 = by shape: the tensor cores from 12288 active rows (n_active x rows)
  *   on, the CUDA cores below; 1 = CUDA cores (weights decoded to f32 in
  *   registers, one f32 FMA each); 2 = tensor cores (the e2m1 codes fed to
  *   tcgen05.mma kind::f8f6f4 as stored, x as five e4m3 planes per scale

@@ -242,7 +242,7 @@ def test_fused_kernels_agree(ops, c5):
 
 
 def test_fused_default_routes_by_shape(ops):
-    """The by-shape default gives the CUDA-core kernel's bits below 16384
+    """The by-shape default gives the CUDA-core kernel's bits below 12288
     active rows and the tensor-core kernel's bits from there on."""
     small = synth.nvfp4_case(8, 256, 1024, 2, seed=83)          # 512 active rows
     large = synth.nvfp4_case(16, 2048, 512, 16, seed=84)        # 32768 active rows
