@@ -757,6 +757,7 @@ def run_profile_workload(args):
     device = torch.device("cuda", 0)
     torch.cuda.set_device(device)
     ops.set_tensor_core_min_m(args.tensor_core_min_m, args.tensor_core_min_bytes)
+    ops.set_fp4_kernel(args.fp4_kernel)
     if args.profile_workload == "mxfp4_experts_6of64_2048x4096":
         st = setup_mxfp4(device)
     elif args.profile_workload.startswith("nvfp4_experts_6of64_2048x4096"):
@@ -785,6 +786,8 @@ def main():
     ap.add_argument("--profile-workload", default=None,
                     help="run --calls calls of this workload and exit (for ncu captures)")
     ap.add_argument("--calls", type=int, default=6)
+    ap.add_argument("--fp4-kernel", type=int, default=0, choices=(0, 1, 2),
+                    help="with --profile-workload: FP4 expert kernel (0 by shape, 1 CUDA cores, 2 tensor cores)")
     ap.add_argument("--tensor-core-min-m", type=int, default=0,
                     help="e4m3 GEMVs with m >= this use the tensor-core kernel (9 = never, 0 = library default)")
     ap.add_argument("--tensor-core-min-bytes", type=int, default=0,
