@@ -106,15 +106,33 @@ TRAFFIC_SOURCES = {
 }
 
 
+def _code_only(text: str) -> str:
+    """C++ source without // comments, trailing blanks and empty lines: what
+    the compiler sees, so that editing a comment keeps a kernel's hash."""
+    out = []
+    for line in text.splitlines():
+        in_str, cut = False, len(line)
+        for i, ch in enumerate(line):
+            if ch == '"' and (i == 0 or line[i - 1] != "\\"):
+                in_str = not in_str
+            elif not in_str and line.startswith("//", i):
+                cut = i
+                break
+        code = line[:cut].rstrip()
+        if code:
+            out.append(code)
+    return "\n".join(out)
+
+
 def source_hash(names=KERNEL_SOURCES) -> str:
-    """Hash of kernel sources (all of them by default); a committed ncu traffic
-    figure is reported only while its workload's sources match (i.e. while the
-    kernel is the one profiled)."""
+    """Hash of kernel sources (all of them by default), comments left out; a
+    committed ncu traffic figure is reported only while its workload's sources
+    match (i.e. while the kernel is the one profiled)."""
     h = hashlib.sha1()
     for name in names:
-        with open(os.path.join(CSRC, name), "rb") as f:
+        with open(os.path.join(CSRC, name), encoding="utf-8") as f:
             h.update(name.encode())
-            h.update(f.read())
+            h.update(_code_only(f.read()).encode())
     return h.hexdigest()[:12]
 
 

@@ -1,13 +1,16 @@
-// fp4tc_gemv.cuh -- NVFP4 routed-expert GEMV on the fifth-generation tensor
-// cores, all active experts in one launch, the e2m1 codes fed to the MMA as
-// stored:
+// fp4tc_gemv.cuh -- NVFP4 and OCP MXFP4 routed-expert GEMV on the
+// fifth-generation tensor cores, all active experts in one launch, the e2m1
+// codes fed to the MMA as stored:
 //   y[k][r] = g[e] * sum_b s[e][r][b] * sum_{c in block b} e2m1(q[e][r][c]) x[c],
-//   e = ids[k], blocks of 16 columns, s = e4m3.
-// Source: "Module dsv4_gpu" page, module header and enum ExpertArm (routed
-// experts stay NVFP4 as stored; each activated expert's weights take the exact
-// values of their dequantisation; one launch per projection, expert ids on
-// the device).  The sum is the one the CUDA-core kernel forms, grouped by
-// scale block.
+//   e = ids[k]; NVFP4: blocks of 16 columns, s = e4m3; MXFP4: blocks of 32,
+//   s = 2^(e8m0 - 127), g = 1.
+// Source: "Module dsv4_gpu" page, module header and enums ExpertArm /
+// ExpertKind (routed experts stay NVFP4 as stored, the MTP block's are OCP
+// MXFP4; each activated expert's weights take the exact values of their
+// dequantisation; one launch per projection, expert ids on the device).  The
+// sum is the one the CUDA-core kernel forms, grouped by scale block.  The
+// description below is NVFP4's; MXFP4 has one block per K = 32 step (B rows
+// 0-4) and a scale-ring slot per stage pair.
 //
 // A (M = 128 weight rows x K): the packed codes.  A 2-D TMA box of 128 e2m1
 //   columns with the 16 x U4 / 16-byte-aligned element type writes each 8
@@ -46,10 +49,10 @@
 //               allocates and frees tensor memory;
 //   warp 8      TMA producer (one lane);
 //   warps 9-12  MMA issuers (one lane each): warp 9 + i issues the eight
-//               steps of every stage g with g % 4 == i, into D stage i (a
-//               thread issues tcgen05 ops at about 100 ns each, so four
-//               threads on whole stages, two commits per stage, beat any
-//               split of a stage's steps).
+//               steps of every stage g with g % 4 == i, into D stage i (one
+//               thread takes about 0.4 us for a stage's MMAs and two
+//               commits; four threads on whole stages were measured faster
+//               than any split of a stage's steps).
 // An expert id outside [0, n_experts) or an unusable global scale makes the
 // slot's outputs NaN and sets FP8BLK_STATUS_BAD_EXPERT; an inf or NaN in x
 // makes every output NaN (the exact sums are not finite).  Every wait is
