@@ -330,11 +330,11 @@ int fp8blk_set_m1_kernel(int choice, int64_t rowwarp_min_bytes);
  *   registers, one f32 FMA each); 2 = tensor cores (the e2m1 codes fed to
  *   tcgen05.mma kind::f8f6f4 as stored, x as five e4m3 planes per scale
  *   block -- 16 columns NVFP4, 32 MXFP4 -- the block scales applied to the
- *   f32 block sums).  The tensor
- *   cores also need 32-byte-aligned codes and room in shared memory for x's
- *   planes (16 bytes per column) beside three stages (cols up to 6656 with
- *   128-row slabs), else the CUDA cores serve the call; with an inf or NaN in
- *   x they return NaN in every output, the CUDA cores the IEEE result.
+ *   f32 block sums).  The tensor cores also need 32-byte-aligned codes and
+ *   room in shared memory for x's planes (16 bytes per column) beside four
+ *   code stages (cols up to 4608 with 128-row slabs, more with shorter ones),
+ *   else the CUDA cores serve the call; with an inf or NaN in x they return
+ *   NaN in every output, the CUDA cores the IEEE result.
  *   Errors: EINVAL.
  */
 int fp8blk_set_fp4_kernel(int choice);
