@@ -201,3 +201,16 @@ def test_mxfp4_zero_block_under_large_scale_and_x(ops, fp4k):
     ref, a = oracle.mxfp4_expert_gemv(case.codes, case.scales, case.ids, x, nthreads=8)
     assert np.isfinite(ref).all() and np.isfinite(y).all()
     assert_close(y, ref, a, "mxfp4 zero block, scale 2^127, x 1e6")
+
+
+def test_mxfp4_sign_and_power_of_two_invariants(ops, fp4k):
+    """Bit-exact on both kernels: y(-x) = -y(x); x * 2^k gives y * 2^k; every
+    e8m0 scale code + k gives y * 2^k."""
+    case = synth.mxfp4_case(4, 300, 1024, 3, seed=98)
+    y = run(ops, case)
+    assert np.array_equal(run(ops, case, x=-case.x).view(np.uint32), (-y).view(np.uint32))
+    for k in (-3, 5):
+        xs = (case.x * np.float32(2.0 ** k)).astype(np.float32)
+        assert np.array_equal(run(ops, case, x=xs), y * np.float32(2.0 ** k)), k
+        shifted = synth.Mxfp4Case(case.codes, (case.scales.astype(np.int32) + k).astype(np.uint8), case.ids, case.x)
+        assert np.array_equal(run(ops, shifted), y * np.float32(2.0 ** k)), k

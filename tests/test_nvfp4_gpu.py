@@ -313,3 +313,20 @@ def test_tensor_core_kernels_back_to_back(ops):
     finally:
         ops.set_fp4_kernel(0)
     assert ops.fp8blk_device_status(clear=True) == 0
+
+
+def test_fused_sign_and_power_of_two_invariants(ops, fp4k):
+    """Bit-exact on both kernels: y(-x) = -y(x); x * 2^k gives y * 2^k; a
+    global scale times 2^k gives y * 2^k (every product and sum scales
+    exactly, so the rounding is the same)."""
+    case = synth.nvfp4_case(4, 300, 1024, 3, seed=97)
+    y = fused(ops, case)
+    neg = fused(ops, synth.Nvfp4Case(case.codes, case.scales, case.gscale, case.ids, -case.x))
+    assert np.array_equal(neg.view(np.uint32), (-y).view(np.uint32))
+    for k in (-3, 5):
+        xs = (case.x * np.float32(2.0 ** k)).astype(np.float32)
+        yx = fused(ops, synth.Nvfp4Case(case.codes, case.scales, case.gscale, case.ids, xs))
+        assert np.array_equal(yx, y * np.float32(2.0 ** k)), k
+        gs = (np.asarray(case.gscale, dtype=np.float32) * np.float32(2.0 ** k)).astype(np.float32)
+        yg = fused(ops, case, gscale=gs)
+        assert np.array_equal(yg, y * np.float32(2.0 ** k)), k
